@@ -1,0 +1,355 @@
+"""Throughput benchmark of the SSD chunked-scan forward on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one ssd_fwd call over the whole workload (default: the Mamba-2
+2.7B layer shape, b=4 T=8192 H=80 P=64 N=128 G=1 Q=256, bf16 x/B/C).  Prints
+ONE JSON line (rank 0).  Inputs are seeded synthetic data resident in HBM;
+L2 is flushed (256 MB write) before every timed step and the flush is outside
+the per-step CUDA-event window.
+
+Multi-GPU: one process per GPU (torchrun); every rank runs its own replica
+of the workload (independent batches, no collective on the data path), the
+timed region is bracketed by a barrier and synchronize, and the slowest
+rank's time sets the whole-job throughput ("scaling": "weak").
+
+--impl reference times the fp64 oracle (the CPU baseline) on the host cores
+on a bounded sample of the same workload.
+"""
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "SSD forward tokens/s per layer at Mamba-2 2.7B shape; % of roofline"
+L2_FLUSH_BYTES = 256 << 20
+
+
+# ---------------------------------------------------------------- helpers
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def init_dist(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def reduce_max(value, dist, device=None):
+    """Max of a float over ranks (identity on one rank)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_id), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [s.strip() for s in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = sorted(float(r[1]) for r in rows if r[1].replace(".", "").isdigit())
+        mx = max(float(r[2]) for r in rows if r[2].replace(".", "").isdigit())
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": mx, "reasons": reasons,
+                "samples": len(rows),
+                "power_w_max": max((float(r[3]) for r in rows if r[3].replace(".", "").isdigit()),
+                                   default=None)}
+
+
+# ---------------------------------------------------------------- CPU baseline
+def oracle_sample(w, inp, budget_s, nthreads=None):
+    """Time the fp64 oracle on a bounded sample of workload ``w``.
+
+    The sample is a set of whole (batch, head) streams over the full
+    sequence; layer tokens/s = (streams / H) * T / seconds.
+    """
+    import oracle
+    threads = oracle.threads_used(nthreads or len(os.sched_getaffinity(0)))
+    total = w.b * w.H
+    # calibrate on one stream prefix
+    probe_T = max(1, min(w.T, 2048))
+    t0 = time.perf_counter()
+    oracle.recurrence(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"],
+                      inp["init_state"], streams=[0], t_end=probe_T, nthreads=1)
+    per_stream = (time.perf_counter() - t0) * (w.T / probe_T)
+    n = int(max(1, min(total, round(budget_s * threads / max(per_stream, 1e-6)))))
+    n = max(threads, (n // threads) * threads) if n >= threads else n
+    n = min(n, total)
+    streams = [int(round(i * (total - 1) / max(n - 1, 1))) for i in range(n)]
+    t0 = time.perf_counter()
+    oracle.recurrence(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"],
+                      inp["init_state"], streams=streams, nthreads=threads)
+    sec = time.perf_counter() - t0
+    tok = len(streams) * w.T / w.H
+    return {"value": tok / sec, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": "%d of %d (batch, head) streams over the full T=%d (%.3g layer tokens), fp64, %.1f s"
+                      % (len(streams), total, w.T, tok, sec)}
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, w):
+    import torch
+    import ssd_sequence_mixing_fwd_b300 as ssd
+    from ssd_sequence_mixing_fwd_b300.inputs import algorithmic_bytes, algorithmic_flops, make_inputs
+
+    rank, world, local = dist_env()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist = init_dist(world, "nccl")
+    ssd.load_library()
+
+    host = make_inputs(w, seed=w.seed + rank)
+    pinned = {k: (None if v is None else v.pin_memory()) for k, v in host.items()}
+    d = {k: (None if v is None else v.to(dev)) for k, v in host.items()}
+    dims = ssd.make_dims(w.b, w.T, w.H, w.P, w.N, w.G, w.Q, w.a_mode, w.dtype)
+    path = ssd.ssd_fwd_path(dims)
+    ws = torch.empty(max(ssd.ssd_fwd_workspace_size(dims), 256), device=dev, dtype=torch.uint8)
+    y = torch.empty_like(d["x"])
+    fin = torch.empty((w.b, w.H, w.N, w.P), device=dev, dtype=torch.float32)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, device=dev, dtype=torch.float32)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ssd.ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["init_state"], chunk_Q=w.Q,
+                    y=y, final_state=fin, workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    st = ssd.ssd_check_device_status(ws, stream)
+    if st != 0:
+        raise ssd.SSDError(st, "warm-up")
+
+    # per-step events around the call, and around the dominant kernel
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    for e in ev:
+        for x in e:
+            x.record(stream)
+    torch.cuda.synchronize(dev)
+    gpu_id = local
+    try:
+        gpu_id = str(torch.cuda.get_device_properties(dev).uuid)
+        gpu_id = gpu_id if gpu_id.startswith("GPU-") else "GPU-" + gpu_id
+    except Exception:
+        pass
+    launches0 = ssd.ssd_launch_count()
+    with ClockSampler(gpu_id) as clk:
+        barrier(dist, dev)
+        torch.cuda.synchronize(dev)
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(1.0)
+            ssd.ssd_debug_set_kernel_events(ev[i][2], ev[i][3])
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        ssd.ssd_debug_set_kernel_events(None, None)
+        torch.cuda.synchronize(dev)
+        barrier(dist, dev)
+        wall = time.perf_counter() - wall0
+    launches = ssd.ssd_launch_count() - launches0
+    st = ssd.ssd_check_device_status(ws, stream)
+    if st != 0:
+        raise ssd.SSDError(st, "timed region")
+    step_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
+    kern_ms = sum(e[2].elapsed_time(e[3]) for e in ev) / args.steps
+    step_ms_max = reduce_max(step_ms, dist, dev)
+    kern_ms_max = reduce_max(kern_ms, dist, dev)
+
+    # end to end: pinned host -> device, the call, device -> pinned host, every step
+    h2d = sum(v.numel() * v.element_size() for v in pinned.values() if v is not None)
+    y_host = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+    f_host = torch.empty(fin.shape, dtype=fin.dtype, pin_memory=True)
+    d2h = y_host.numel() * y_host.element_size() + f_host.numel() * f_host.element_size()
+
+    def e2e_step():
+        for k, v in pinned.items():
+            if v is not None:
+                d[k].copy_(v, non_blocking=True)
+        step()
+        y_host.copy_(y, non_blocking=True)
+        f_host.copy_(fin, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_e2e = max(3, min(args.steps, 10))
+    barrier(dist, dev)
+    e0.record(stream)
+    for _ in range(n_e2e):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = reduce_max(e0.elapsed_time(e1) / n_e2e, dist, dev)
+
+    tokens = w.tokens
+    value = tokens * world / (step_ms_max / 1e3)
+    peaks = load_peaks()
+    by = algorithmic_bytes(w)
+    fl = algorithmic_flops(w)
+    achieved = by / (kern_ms / 1e3) / 1e9
+    out = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16-mma/f32" if path == "tcgen05" else "f32", "data": "synthetic",
+        "config": {"workload": w.name, "b": w.b, "T": w.T, "H": w.H, "P": w.P, "N": w.N, "G": w.G,
+                   "Q": w.Q, "a_mode": w.a_mode, "io_dtype": w.dtype, "path": path,
+                   "global_batch": w.b * world, "seq_len": w.T, "parallelism": "replicas x%d" % world,
+                   "l2": "flushed (256 MB write) before every timed step"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                     "kernel_ms": kern_ms, "algorithmic_bytes": by,
+                     "peak_note": "hbm_gbs of %s peaks (burst copy)" % peaks["source"],
+                     "tensor_tflops": fl / (kern_ms / 1e3) / 1e12,
+                     "tensor_frac": fl / (kern_ms / 1e3) / 1e12 / peaks["bf16_tflops"],
+                     "step_frac": (by / peaks["hbm_gbs"] / 1e9) / (step_ms_max / 1e3)},
+        "e2e": {"value": tokens * world / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+        "wall_s_timed": wall,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = oracle_sample(w, host, args.cpu_budget)
+    if dist is not None:
+        dist.destroy_process_group()
+    return out if rank == 0 else None
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args, w):
+    """The fp64 oracle, as it stands, timed on the host cores (rank 0 only)."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    from ssd_sequence_mixing_fwd_b300.inputs import make_inputs
+    import oracle
+    inp = make_inputs(w)
+    threads = oracle.threads_used(len(os.sched_getaffinity(0)))
+    total = w.b * w.H
+    # each step: `threads` whole streams over the full sequence (bounded)
+    n = min(total, threads)
+    per_step_tok = n * w.T / w.H
+    times = []
+    for i in range(args.warmup + args.steps):
+        streams = [((i * n + k) * 7919) % total for k in range(n)]
+        t0 = time.perf_counter()
+        oracle.recurrence(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"],
+                          inp["init_state"], streams=streams, nthreads=threads)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    sec = sum(times) / len(times)
+    v = per_step_tok / sec
+    return {"metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": w.name, "b": w.b, "T": w.T, "H": w.H, "P": w.P, "N": w.N,
+                       "G": w.G, "Q": w.Q, "a_mode": w.a_mode, "io_dtype": w.dtype},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                             "sample": "per step %d of %d (batch, head) streams over the full T=%d"
+                                       % (n, total, w.T)},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    from ssd_sequence_mixing_fwd_b300.inputs import WORKLOADS
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="mamba2_2p7b", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)        # at least 3 untimed warm-up steps
+    w = WORKLOADS[args.workload]
+    out = run_reference(args, w) if args.impl == "reference" else run_ours(args, w)
+    if out is not None:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

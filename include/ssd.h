@@ -1,0 +1,162 @@
+/*
+ * ssd.h -- C ABI of libssd_b300.so, the B300 (sm_103a) forward pass of the
+ * SSD chunked scan, the sequence-mixing layer of Mamba-2.
+ *
+ * The operation (Structured State Space Duality, "The recurrence as one
+ * matrix"; scalar-times-identity decay as in the same section; the general
+ * diagonal decay of "What the duality gives up" and of "On Structured
+ * State-Space Duality", abstract, point (i)):
+ *
+ *   for every batch row bi and head h, with g = h / (H / G):
+ *     h_{-1} = init_state[bi,h]                      (zero when NULL)
+ *     a_t    = exp(dt[bi,t,h] * A[h])                (scalar A, shape (H))
+ *     a_t[n] = exp(dt[bi,t,h] * A[h,n])              (diagonal A, shape (H,N))
+ *     h_t    = a_t (.) h_{t-1} + B[bi,t,g,:] x[bi,t,h,:]^T          (N x P)
+ *     y[bi,t,h,:] = C[bi,t,g,:]^T h_t + D[h] x[bi,t,h,:]            (D optional)
+ *     final_state[bi,h] = h_{T-1}
+ *
+ * It is evaluated by the chunked algorithm of the same page ("The chunked
+ * algorithm takes both"): chunks of Q tokens; inside a chunk the decay-masked
+ * quadratic form (C B^T o L) X on tensor cores; across chunks one fp32 state
+ * recurrence step per chunk ("When it breaks": decay sums and state in fp32).
+ * The result equals the recurrence up to rounding for every Q.
+ *
+ * Conventions shared by every entry point
+ *   - All tensor arguments are DEVICE pointers to dense row-major arrays in
+ *     the layouts given below, owned by the caller.  The library allocates no
+ *     memory and keeps no pointer after a call returns.
+ *   - Every pointer must be 16-byte aligned (SSD_ERR_ALIGNMENT otherwise).
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream).  The library never synchronises except in
+ *     ssd_check_device_status.
+ *   - Every function returns an int status (SSD_OK = 0).  All argument checks
+ *     run before anything is enqueued; on any error nothing is enqueued.
+ *   - Not reentrant on one workspace: two calls that share a workspace must be
+ *     ordered on the GPU (same stream or an event between them).
+ */
+#ifndef SSD_B300_H
+#define SSD_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SSD_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define SSD_API __attribute__((visibility("default")))
+#else
+#define SSD_API
+#endif
+
+/* ---- status codes ---------------------------------------------------- */
+#define SSD_OK              0
+#define SSD_ERR_INVALID_ARG 1  /* a size, mode or required pointer is invalid   */
+#define SSD_ERR_UNSUPPORTED 2  /* valid, but outside what this build handles    */
+#define SSD_ERR_ALIGNMENT   3  /* a pointer is not 16-byte aligned              */
+#define SSD_ERR_WORKSPACE   4  /* workspace NULL or smaller than required       */
+#define SSD_ERR_CUDA        5  /* a CUDA runtime/driver call or launch failed   */
+#define SSD_ERR_TIMEOUT     6  /* device side: a bounded inter-CTA wait expired  */
+#define SSD_ERR_DEVICE      7  /* device side: a kernel's own check failed       */
+
+/* ---- modes ----------------------------------------------------------- */
+#define SSD_A_SCALAR   0       /* A has shape (H): a_t = exp(dt_t A_h) I        */
+#define SSD_A_DIAGONAL 1       /* A has shape (H,N): one decay per state dim    */
+
+#define SSD_DTYPE_BF16 0       /* x, B, C, y are bfloat16                       */
+#define SSD_DTYPE_F32  1       /* x, B, C, y are float32                        */
+
+#define SSD_PATH_AUTO     0    /* pick the fastest path that supports the dims   */
+#define SSD_PATH_GENERIC  1    /* CUDA-core fp32 pipeline (any supported dims)   */
+#define SSD_PATH_TCGEN05  2    /* fused tcgen05/TMA kernel (restricted dims)     */
+
+/* Problem description.  Names follow the pages' notation:
+ *   b batch, T sequence length, H heads, P head dim, N state dim,
+ *   G B/C groups (H % G == 0), Q chunk length.
+ * Constraints: b >= 0, T >= 0, H >= 1, G >= 1, H % G == 0,
+ *   1 <= P <= 256 and P a power of two, 1 <= N <= 256, N * P <= 16384,
+ *   Q in {64, 128, 256}.
+ * b == 0 or T == 0 is a valid empty problem: y is empty and final_state is
+ * init_state (or zero).  A ragged last chunk (T % Q != 0) is allowed.
+ * Domain (not checked on the device): dt >= 0 and A <= 0, all finite; the
+ * fused path keeps matrix operands in fp16, so |x|, |B|, |C| and the state
+ * entries must stay below 65504. */
+typedef struct ssd_dims {
+    int64_t b, T, H, P, N, G, Q;
+    int32_t a_mode;    /* SSD_A_SCALAR or SSD_A_DIAGONAL                       */
+    int32_t io_dtype;  /* SSD_DTYPE_BF16 or SSD_DTYPE_F32                      */
+    int32_t path;      /* SSD_PATH_*; SSD_PATH_AUTO unless testing a path      */
+    int32_t reserved;  /* must be 0                                            */
+} ssd_dims;
+
+/* Bytes of device workspace ssd_fwd needs for `dims` (written to *bytes).
+ * Host-only; enqueues nothing.  Returns SSD_ERR_INVALID_ARG /
+ * SSD_ERR_UNSUPPORTED for dims ssd_fwd would reject. */
+SSD_API int ssd_fwd_workspace_size(const ssd_dims *dims, size_t *bytes);
+
+/* The kernel path ssd_fwd would run for `dims` (SSD_PATH_GENERIC or
+ * SSD_PATH_TCGEN05), written to *path.  Host-only. */
+SSD_API int ssd_fwd_path(const ssd_dims *dims, int32_t *path);
+
+/* Forward pass.  Layouts (all dense, row-major, device memory):
+ *   x           (b,T,H,P)  io dtype         read
+ *   dt          (b,T,H)    float32          read
+ *   A           (H) or (H,N) float32        read (per a_mode)
+ *   B, C        (b,T,G,N)  io dtype         read
+ *   D           (H)        float32 or NULL  read; NULL = no skip term
+ *   init_state  (b,H,N,P)  float32 or NULL  read; NULL = zero state
+ *   y           (b,T,H,P)  io dtype         written
+ *   final_state (b,H,N,P)  float32 or NULL  written; NULL = not returned
+ *   workspace   >= ssd_fwd_workspace_size bytes, device memory, 256-byte
+ *               aligned; scratch owned by the caller, contents need no
+ *               initialisation and are undefined after the call.
+ * y must not alias any input.  Returns after enqueueing the kernels on
+ * `stream`; errors found on the device (SSD_ERR_TIMEOUT, SSD_ERR_DEVICE)
+ * are reported by ssd_check_device_status. */
+SSD_API int ssd_fwd(const ssd_dims *dims,
+            const void *x, const float *dt, const float *A,
+            const void *B, const void *C, const float *D,
+            const float *init_state,
+            void *y, float *final_state,
+            void *workspace, size_t workspace_bytes,
+            void *stream);
+
+/* Synchronises `stream`, then reads the device-side status word that the
+ * last ssd_fwd on this workspace left, and clears it.  Returns SSD_OK,
+ * SSD_ERR_TIMEOUT (an inter-CTA wait hit its iteration limit; outputs are
+ * invalid), SSD_ERR_DEVICE, or SSD_ERR_CUDA if the stream reported an error. */
+SSD_API int ssd_check_device_status(void *workspace, size_t workspace_bytes, void *stream);
+
+/* Static English text for a status code (never NULL). */
+SSD_API const char *ssd_status_string(int status);
+
+/* SSD_ABI_VERSION of the loaded library. */
+SSD_API int ssd_abi_version(void);
+
+/* Test hook for the failure-detection path of the fused kernel.
+ * spin_limit: iteration limit of each inter-chunk wait (<= 0 restores the
+ * default).  withhold_chunk: when >= 0, the work item of that chunk index
+ * never publishes its state, so its successor's wait must run out and report
+ * SSD_ERR_TIMEOUT through ssd_check_device_status.  Process-wide; not for
+ * production use.  Returns SSD_OK. */
+SSD_API int ssd_debug_set_wait(int64_t spin_limit, int64_t withhold_chunk);
+
+/* Measurement hook.  When both handles are non-NULL (cudaEvent_t values
+ * created by the caller), every later ssd_fwd records `start_event` on its
+ * stream right before it launches its dominant kernel and `stop_event` right
+ * after, so the caller can time that kernel alone with cudaEventElapsedTime.
+ * Pass NULLs to switch it off.  Process-wide.  Returns SSD_OK. */
+SSD_API int ssd_debug_set_kernel_events(void *start_event, void *stop_event);
+
+/* Number of kernels this process has launched through the library so far
+ * (written to *count).  Host-side counter; returns SSD_OK. */
+SSD_API int ssd_launch_count(uint64_t *count);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSD_B300_H */

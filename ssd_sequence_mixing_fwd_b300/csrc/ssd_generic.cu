@@ -1,0 +1,360 @@
+// ssd_generic.cu -- the generic CUDA-core path of the SSD chunked scan.
+//
+// Three kernels, all arithmetic in fp32 (exact fp32 FMA, no tensor cores), for
+// any dims the ABI accepts.  It is the path for fp32 inputs (where the 1e-5
+// tolerance rules out tf32 operands) and for shapes the fused tcgen05 kernel
+// does not take.  The steps are those of Structured State Space Duality, "The
+// chunked algorithm takes both":
+//
+//   gen_chunk_state    per (b, h, chunk): the chunk prefix sums of the log
+//                      decay, and the chunk's input projection
+//                      s_c = B_c^T (w o X_c), w_j = decay from token j to the
+//                      chunk end (the low-rank factor of the off-diagonal
+//                      blocks).
+//   gen_state_passing  per (b, h, n, p): h_c = a_c h_{c-1} + s_c over chunks,
+//                      one recurrence step per chunk, fp32 ("When it breaks");
+//                      leaves h_{c-1} (the state entering chunk c) in place.
+//   gen_chunk_output   per (b, h, chunk, 32-row tile): the diagonal block
+//                      (C B^T o L) X with L_ij = exp(cum_i - cum_j), plus the
+//                      off-diagonal part exp(cum_i) C_i^T h_{c-1}, plus D x.
+//
+// In the diagonal-A variant the decay of state dim n between tokens j <= i is
+// exp(A_{h,n} (S_i - S_j)) with S the chunk prefix sum of dt, so the mask is a
+// sum over n and is formed inside the n loop.
+#include <cuda_bf16.h>
+
+#include "ssd_internal.cuh"
+
+namespace ssd {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kTT = 16;        // tokens per shared-memory tile (chunk state)
+constexpr int kMaxAcc = 64;    // N*P / 256 accumulators per thread at most
+constexpr int kRT = 32;        // output rows per block
+constexpr int kJT = 32;        // key (j) columns per tile
+constexpr int kMaxOut = 32;    // kRT*P / 256 outputs per thread at most
+
+template <typename IO> __device__ __forceinline__ float ld_io(const IO *p, int64_t i);
+template <> __device__ __forceinline__ float ld_io<float>(const float *p, int64_t i) { return p[i]; }
+template <> __device__ __forceinline__ float ld_io<__nv_bfloat16>(const __nv_bfloat16 *p, int64_t i) {
+    return __bfloat162float(p[i]);
+}
+template <typename IO> __device__ __forceinline__ void st_io(IO *p, int64_t i, float v);
+template <> __device__ __forceinline__ void st_io<float>(float *p, int64_t i, float v) { p[i] = v; }
+template <> __device__ __forceinline__ void st_io<__nv_bfloat16>(__nv_bfloat16 *p, int64_t i, float v) {
+    p[i] = __float2bfloat16_rn(v);
+}
+
+// Inclusive prefix sum over the chunk of s_t = dt_t*A_h (scalar) or dt_t
+// (diagonal) into lcum[0..Q); entries past the chunk's length are zero.
+// Hillis-Steele over shared memory; Q <= blockDim.
+__device__ __forceinline__ void chunk_prefix(const Problem &p, int bi, int h, int64_t t0, int L,
+                                             float *lcum) {
+    const int tid = threadIdx.x;
+    float v = 0.f;
+    if (tid < L) {
+        v = p.dt[((int64_t)bi * p.T + t0 + tid) * p.H + h];
+        if (p.a_mode == SSD_A_SCALAR) v *= p.A[h];
+    }
+    if (tid < p.Q) lcum[tid] = v;
+    __syncthreads();
+    for (int off = 1; off < p.Q; off <<= 1) {
+        float add = (tid < p.Q && tid >= off) ? lcum[tid - off] : 0.f;
+        __syncthreads();
+        if (tid < p.Q) lcum[tid] += add;
+        __syncthreads();
+    }
+}
+
+template <typename IO>
+__global__ void __launch_bounds__(kThreads) gen_chunk_state(Problem p, GenericWorkspace w) {
+    extern __shared__ float smem[];
+    const int c = blockIdx.x, h = blockIdx.y, bi = blockIdx.z, tid = threadIdx.x;
+    const int N = (int)p.N, P = (int)p.P;
+    const int64_t t0 = (int64_t)c * p.Q;
+    const int L = (int)min(p.Q, p.T - t0);
+    const int g = h / (int)(p.H / p.G);
+    const IO *X = static_cast<const IO *>(p.x);
+    const IO *Bm = static_cast<const IO *>(p.B);
+
+    float *lcum = smem;                 // Q
+    float *Bw = lcum + p.Q;             // kTT x N
+    float *Xs = Bw + kTT * N;           // kTT x P
+
+    chunk_prefix(p, bi, h, t0, L, lcum);
+    const float total = lcum[L - 1];
+    if (tid == 0) w.chunk_sum[((int64_t)bi * p.H + h) * p.nc + c] = total;
+
+    const int pcol = tid % P;
+    const int n0 = tid / P;
+    const int nstep = kThreads / P;
+    const int nacc = (N + nstep - 1) / nstep;
+    float acc[kMaxAcc];
+#pragma unroll
+    for (int a = 0; a < kMaxAcc; ++a) acc[a] = 0.f;
+
+    for (int tt = 0; tt < L; tt += kTT) {
+        for (int e = tid; e < kTT * N; e += kThreads) {
+            const int k = e / N, n = e % N;
+            float v = 0.f;
+            if (tt + k < L) {
+                const int64_t tok = (int64_t)bi * p.T + t0 + tt + k;
+                const float d = total - lcum[tt + k];
+                const float lw = (p.a_mode == SSD_A_SCALAR) ? d : p.A[(int64_t)h * N + n] * d;
+                v = ld_io(Bm, (tok * p.G + g) * N + n) * expf(lw);
+            }
+            Bw[e] = v;
+        }
+        for (int e = tid; e < kTT * P; e += kThreads) {
+            const int k = e / P, pp = e % P;
+            float v = 0.f;
+            if (tt + k < L) {
+                const int64_t tok = (int64_t)bi * p.T + t0 + tt + k;
+                v = ld_io(X, (tok * p.H + h) * P + pp);
+            }
+            Xs[e] = v;
+        }
+        __syncthreads();
+        if (n0 < nstep) {
+#pragma unroll 4
+            for (int k = 0; k < kTT; ++k) {
+                const float xv = Xs[k * P + pcol];
+#pragma unroll
+                for (int a = 0; a < kMaxAcc; ++a) {
+                    const int n = n0 + a * nstep;
+                    if (a < nacc && n < N) acc[a] = fmaf(Bw[k * N + n], xv, acc[a]);
+                }
+            }
+        }
+        __syncthreads();
+    }
+    float *out = w.states + (((int64_t)bi * p.H + h) * p.nc + c) * N * P;
+#pragma unroll
+    for (int a = 0; a < kMaxAcc; ++a) {
+        const int n = n0 + a * nstep;
+        if (a < nacc && n < N && n0 < nstep) out[(int64_t)n * P + pcol] = acc[a];
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) gen_state_passing(Problem p, GenericWorkspace w) {
+    const int h = blockIdx.y, bi = blockIdx.z;
+    const int64_t NP = p.N * p.P;
+    const int64_t o = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    if (o >= NP) return;
+    const int n = (int)(o / p.P);
+    const int64_t bh = (int64_t)bi * p.H + h;
+    float hs = p.init ? p.init[bh * NP + o] : 0.f;
+    float *st = w.states + bh * p.nc * NP + o;
+    const float *cs = w.chunk_sum + bh * p.nc;
+    const float An = (p.a_mode == SSD_A_SCALAR) ? 1.f : p.A[(int64_t)h * p.N + n];
+    for (int64_t c = 0; c < p.nc; ++c) {
+        const float s = st[c * NP];
+        st[c * NP] = hs;                       // state entering chunk c
+        const float a = expf(An * cs[c]);      // decay across the whole chunk
+        hs = fmaf(a, hs, s);
+    }
+    if (p.final_state) p.final_state[bh * NP + o] = hs;
+}
+
+template <typename IO>
+__global__ void __launch_bounds__(kThreads) gen_chunk_output(Problem p, GenericWorkspace w) {
+    extern __shared__ float smem[];
+    const int nrt = (int)((p.Q + kRT - 1) / kRT);
+    const int c = blockIdx.x / nrt, rt = blockIdx.x % nrt;
+    const int h = blockIdx.y, bi = blockIdx.z, tid = threadIdx.x;
+    const int N = (int)p.N, P = (int)p.P;
+    const int64_t t0 = (int64_t)c * p.Q;
+    const int L = (int)min(p.Q, p.T - t0);
+    const int i0 = rt * kRT;
+    if (i0 >= L) return;                       // uniform over the block
+    const int g = h / (int)(p.H / p.G);
+    const IO *X = static_cast<const IO *>(p.x);
+    const IO *Bm = static_cast<const IO *>(p.B);
+    const IO *Cm = static_cast<const IO *>(p.C);
+    const int NS = N + 1;                      // padded row stride
+
+    float *lcum = smem;                        // Q
+    float *As = lcum + p.Q;                    // N
+    float *Cs = As + N;                        // kRT x NS
+    float *Bs = Cs + kRT * NS;                 // kJT x NS
+    float *Xs = Bs + kJT * NS;                 // kJT x P
+    float *Ss = Xs + kJT * P;                  // kRT x (kJT+1)
+    float *Hs = Ss + kRT * (kJT + 1);          // kJT x P
+
+    chunk_prefix(p, bi, h, t0, L, lcum);
+    for (int n = tid; n < N; n += kThreads)
+        As[n] = (p.a_mode == SSD_A_SCALAR) ? 1.f : p.A[(int64_t)h * N + n];
+    for (int e = tid; e < kRT * N; e += kThreads) {
+        const int r = e / N, n = e % N;
+        float v = 0.f;
+        if (i0 + r < L) v = ld_io(Cm, (((int64_t)bi * p.T + t0 + i0 + r) * p.G + g) * N + n);
+        Cs[r * NS + n] = v;
+    }
+    __syncthreads();
+
+    const int pcol = tid % P;
+    const int r0 = tid / P;
+    const int rstep = kThreads / P;            // >= 1 since P <= 256
+    const int nout = (kRT + rstep - 1) / rstep;
+    float acc[kMaxOut];
+#pragma unroll
+    for (int a = 0; a < kMaxOut; ++a) acc[a] = 0.f;
+
+    const int i_last = min(i0 + kRT, L) - 1;
+    for (int j0 = 0; j0 <= i_last; j0 += kJT) {
+        for (int e = tid; e < kJT * N; e += kThreads) {
+            const int k = e / N, n = e % N;
+            float v = 0.f;
+            if (j0 + k < L) v = ld_io(Bm, (((int64_t)bi * p.T + t0 + j0 + k) * p.G + g) * N + n);
+            Bs[k * NS + n] = v;
+        }
+        for (int e = tid; e < kJT * P; e += kThreads) {
+            const int k = e / P, pp = e % P;
+            float v = 0.f;
+            if (j0 + k < L) v = ld_io(X, (((int64_t)bi * p.T + t0 + j0 + k) * p.H + h) * P + pp);
+            Xs[e] = v;
+        }
+        __syncthreads();
+        for (int e = tid; e < kRT * kJT; e += kThreads) {
+            const int r = e / kJT, k = e % kJT;
+            const int i = i0 + r, j = j0 + k;
+            float v = 0.f;
+            if (j <= i && i < L) {
+                const float dlt = lcum[i] - lcum[j];
+                const float *cr = Cs + r * NS;
+                const float *br = Bs + k * NS;
+                if (p.a_mode == SSD_A_SCALAR) {
+                    float dot = 0.f;
+                    for (int n = 0; n < N; ++n) dot = fmaf(cr[n], br[n], dot);
+                    v = dot * expf(dlt);
+                } else {
+                    for (int n = 0; n < N; ++n) v = fmaf(cr[n] * br[n], expf(As[n] * dlt), v);
+                }
+            }
+            Ss[r * (kJT + 1) + k] = v;
+        }
+        __syncthreads();
+        if (r0 < rstep) {
+#pragma unroll
+            for (int a = 0; a < kMaxOut; ++a) {
+                const int r = r0 + a * rstep;
+                if (a < nout && r < kRT) {
+                    float s = acc[a];
+                    for (int k = 0; k < kJT; ++k) s = fmaf(Ss[r * (kJT + 1) + k], Xs[k * P + pcol], s);
+                    acc[a] = s;
+                }
+            }
+        }
+        __syncthreads();
+    }
+
+    // Off-diagonal blocks: exp(cum_i) C_i^T h_{c-1}; fold the decay into C.
+    for (int e = tid; e < kRT * N; e += kThreads) {
+        const int r = e / N, n = e % N;
+        const int i = i0 + r;
+        if (i < L) Cs[r * NS + n] *= expf(As[n] * lcum[i]);
+    }
+    const float *hprev = w.states + (((int64_t)bi * p.H + h) * p.nc + c) * N * P;
+    for (int nb0 = 0; nb0 < N; nb0 += kJT) {
+        __syncthreads();
+        for (int e = tid; e < kJT * P; e += kThreads) {
+            const int k = e / P;
+            Hs[e] = (nb0 + k < N) ? hprev[(int64_t)(nb0 + k) * P + (e % P)] : 0.f;
+        }
+        __syncthreads();
+        const int kmax = min(kJT, N - nb0);
+        if (r0 < rstep) {
+#pragma unroll
+            for (int a = 0; a < kMaxOut; ++a) {
+                const int r = r0 + a * rstep;
+                if (a < nout && r < kRT) {
+                    float s = acc[a];
+                    for (int k = 0; k < kmax; ++k) s = fmaf(Cs[r * NS + nb0 + k], Hs[k * P + pcol], s);
+                    acc[a] = s;
+                }
+            }
+        }
+    }
+
+    IO *Y = static_cast<IO *>(p.y);
+    const float Dh = p.D ? p.D[h] : 0.f;
+    if (r0 < rstep) {
+#pragma unroll
+        for (int a = 0; a < kMaxOut; ++a) {
+            const int r = r0 + a * rstep;
+            const int i = i0 + r;
+            if (a < nout && r < kRT && i < L) {
+                const int64_t off = (((int64_t)bi * p.T + t0 + i) * p.H + h) * P + pcol;
+                float v = acc[a];
+                if (p.D) v = fmaf(Dh, ld_io(X, off), v);
+                st_io(Y, off, v);
+            }
+        }
+    }
+}
+
+size_t state_smem(const Problem &p) { return sizeof(float) * (p.Q + kTT * p.N + kTT * p.P); }
+size_t output_smem(const Problem &p) {
+    const size_t NS = p.N + 1;
+    return sizeof(float) * (p.Q + p.N + kRT * NS + kJT * NS + kJT * p.P + kRT * (kJT + 1) + kJT * p.P);
+}
+
+template <typename IO>
+cudaError_t launch_typed(const Problem &p, const GenericWorkspace &w, cudaStream_t s) {
+    const size_t sm1 = state_smem(p), sm3 = output_smem(p);
+    cudaError_t e;
+    if ((e = cudaFuncSetAttribute(gen_chunk_state<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)sm1)) != cudaSuccess)
+        return e;
+    if ((e = cudaFuncSetAttribute(gen_chunk_output<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)sm3)) != cudaSuccess)
+        return e;
+    dim3 g1((unsigned)p.nc, (unsigned)p.H, (unsigned)p.b);
+    gen_chunk_state<IO><<<g1, kThreads, sm1, s>>>(p, w);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    dim3 g2((unsigned)((p.N * p.P + kThreads - 1) / kThreads), (unsigned)p.H, (unsigned)p.b);
+    gen_state_passing<<<g2, kThreads, 0, s>>>(p, w);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const int64_t nrt = (p.Q + kRT - 1) / kRT;
+    dim3 g3((unsigned)(p.nc * nrt), (unsigned)p.H, (unsigned)p.b);
+    record_dominant_start(s);
+    gen_chunk_output<IO><<<g3, kThreads, sm3, s>>>(p, w);
+    record_dominant_stop(s);
+    note_launches(3);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool generic_supports(const Problem &p) {
+    if (p.P < 1 || p.P > 256 || (p.P & (p.P - 1))) return false;
+    if (p.N < 1 || p.N > 256 || p.N * p.P > (int64_t)kMaxAcc * kThreads) return false;
+    if (p.Q > kThreads) return false;
+    if (kRT * p.P > (int64_t)kMaxOut * kThreads) return false;
+    return output_smem(p) <= 227 * 1024;
+}
+
+size_t generic_workspace_bytes(const Problem &p) {
+    size_t off = kStatusBytes;
+    off += align_up(sizeof(float) * (size_t)(p.b * p.H * p.nc), 256);
+    off += sizeof(float) * (size_t)(p.b * p.H * p.nc * p.N * p.P);
+    return off;
+}
+
+GenericWorkspace generic_carve(const Problem &p, void *ws) {
+    char *base = static_cast<char *>(ws);
+    GenericWorkspace w;
+    w.status = reinterpret_cast<int *>(base);
+    w.chunk_sum = reinterpret_cast<float *>(base + kStatusBytes);
+    w.states = reinterpret_cast<float *>(base + kStatusBytes +
+                                         align_up(sizeof(float) * (size_t)(p.b * p.H * p.nc), 256));
+    return w;
+}
+
+cudaError_t generic_launch(const Problem &p, const GenericWorkspace &w, cudaStream_t s) {
+    if (p.io_dtype == SSD_DTYPE_BF16) return launch_typed<__nv_bfloat16>(p, w, s);
+    return launch_typed<float>(p, w, s);
+}
+
+}  // namespace ssd

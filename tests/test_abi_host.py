@@ -1,0 +1,118 @@
+"""Host-side checks of the C ABI (no GPU needed, no compute calls).
+
+The library must load, export every function include/ssd.h declares, and
+reject bad arguments before touching the GPU.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import ssd_sequence_mixing_fwd_b300 as ssd
+from ssd_sequence_mixing_fwd_b300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return ssd.load_library()
+
+
+def declared_functions():
+    names = []
+    for hdr in os.listdir(os.path.join(ROOT, "include")):
+        if hdr.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", hdr)).read()
+            names += re.findall(r"^SSD_API\s+[\w\s\*]*?\b(\w+)\s*\(", text, re.M)
+    return names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert "ssd_fwd" in names and len(names) >= 7
+    for n in names:
+        assert hasattr(lib, n), n
+    for n in ssd.EXPORTED:
+        assert n in names
+
+
+def test_abi_version_and_status_strings(lib):
+    assert ssd.ssd_abi_version() == 1
+    for st in range(0, 8):
+        assert isinstance(ssd.ssd_status_string(st), str)
+    assert ssd.ssd_status_string(99) == "unknown status"
+
+
+def dims(**kw):
+    base = dict(b=2, T=1000, H=4, P=64, N=128, G=2, Q=128)
+    base.update(kw)
+    return ssd.make_dims(**base)
+
+
+def test_workspace_size_matches_layout(lib):
+    d = dims()
+    n = ssd.ssd_fwd_workspace_size(dims(path="generic"))
+    nc = (1000 + 127) // 128
+    states = 2 * 4 * nc * 128 * 64 * 4
+    assert n >= states and n < states + 4096 + 2 * 4 * nc * 4 + 256
+    assert ssd.ssd_fwd_workspace_size(d) > 0
+
+
+@pytest.mark.parametrize("bad", [
+    dict(H=3, G=2),          # H % G != 0
+    dict(Q=96),              # chunk length not supported
+    dict(Q=0),
+    dict(T=-1),
+    dict(b=-2),
+    dict(P=0),
+    dict(N=0),
+    dict(G=0),
+])
+def test_invalid_dims_rejected(lib, bad):
+    with pytest.raises(ssd.SSDError) as e:
+        ssd.ssd_fwd_workspace_size(dims(**bad))
+    assert e.value.status == ssd.SSD_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("bad", [dict(P=48), dict(P=512), dict(N=300), dict(N=256, P=128)])
+def test_unsupported_dims_rejected(lib, bad):
+    with pytest.raises(ssd.SSDError) as e:
+        ssd.ssd_fwd_workspace_size(dims(**bad))
+    assert e.value.status == ssd.SSD_ERR_UNSUPPORTED
+
+
+def test_bad_mode_values_rejected(lib):
+    for field, val in (("a_mode", 5), ("io_dtype", 9), ("path", 7), ("reserved", 1)):
+        d = dims()
+        setattr(d, field, val)
+        n = ctypes.c_size_t(0)
+        assert lib.ssd_fwd_workspace_size(ctypes.byref(d), ctypes.byref(n)) == ssd.SSD_ERR_INVALID_ARG
+
+
+def test_null_and_misaligned_pointers_rejected_before_any_launch(lib):
+    d = dims(path="generic")
+    ws = ctypes.c_void_p(1 << 20)
+    args = [ctypes.c_void_p((1 << 21) + 4096 * i) for i in range(9)]
+    # required pointer missing
+    a = list(args)
+    a[0] = None
+    assert lib.ssd_fwd(ctypes.byref(d), *a, ws, 1 << 40, None) == ssd.SSD_ERR_INVALID_ARG
+    # misaligned x
+    a = list(args)
+    a[0] = ctypes.c_void_p((1 << 21) + 2)
+    assert lib.ssd_fwd(ctypes.byref(d), *a, ws, 1 << 40, None) == ssd.SSD_ERR_ALIGNMENT
+    # workspace too small / missing
+    assert lib.ssd_fwd(ctypes.byref(d), *args, ws, 16, None) == ssd.SSD_ERR_WORKSPACE
+    assert lib.ssd_fwd(ctypes.byref(d), *args, None, 1 << 40, None) == ssd.SSD_ERR_WORKSPACE
+    # y aliasing x
+    a = list(args)
+    a[7] = a[0]
+    assert lib.ssd_fwd(ctypes.byref(d), *a, ws, 1 << 40, None) == ssd.SSD_ERR_INVALID_ARG
+
+
+def test_path_query(lib):
+    assert ssd.ssd_fwd_path(dims(path="generic")) == "generic"
+    assert ssd.ssd_fwd_path(dims(dtype="f32")) in ("generic", "tcgen05")
