@@ -309,3 +309,24 @@ def test_planted_mistakes_are_caught(plant):
 
 def test_oracle_reports_threads():
     assert oracle.threads_used(2) == 2
+
+
+@pytest.mark.parametrize("name", ["tiny_scalar_T3.txt", "tiny_diagonal_T3.txt"])
+def test_brute_force_forms_match_hand_worked_examples(name):
+    """Pins the dense-M and masked-attention code itself to the hand-worked values."""
+    g = _read_golden(name)
+    N = int(g["N"][0])
+    vals = lambda k: np.array([float(v) for v in g[k]])
+    x, dt, A = vals("x").reshape(3, 1), vals("dt"), vals("A").astype(np.float32).astype(np.float64)
+    B, C = vals("B").reshape(3, N), vals("C").reshape(3, N)
+    a = np.exp(dt[:, None] * A[None, :]) if g["a_mode"][0] == "diagonal" else np.exp(dt * A[0])
+    M = brute.dense_M(a, B, C)
+    y = brute.apply_M(M, x, a, C, vals("init_state").reshape(N, 1), float(g["D"][0]))
+    np.testing.assert_allclose(y.ravel(), vals("y"), rtol=1e-7, atol=1e-8)
+    h = brute.final_state_from_M(x, a, B, vals("init_state").reshape(N, 1))
+    np.testing.assert_allclose(h.ravel(), vals("final_state"), rtol=1e-7, atol=1e-8)
+    if g["a_mode"][0] == "scalar":
+        # with zero initial state the single-mask form gives y minus the decayed-h0 term
+        y0 = brute.apply_M(M, x, a, C, None, float(g["D"][0]))
+        ya = brute.masked_attention(x, a, B, C, float(g["D"][0]))
+        np.testing.assert_allclose(ya, y0, rtol=1e-14, atol=1e-14)
