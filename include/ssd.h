@@ -61,6 +61,7 @@ extern "C" {
 #define SSD_ERR_CUDA        5  /* a CUDA runtime/driver call or launch failed   */
 #define SSD_ERR_TIMEOUT     6  /* device side: a bounded inter-CTA wait expired  */
 #define SSD_ERR_DEVICE      7  /* device side: a kernel's own check failed       */
+#define SSD_ERR_SCRATCH_LIMIT 8 /* ssd_fwd_noalloc: problem exceeds its scratch  */
 
 /* ---- modes ----------------------------------------------------------- */
 #define SSD_A_SCALAR   0       /* A has shape (H): a_t = exp(dt_t A_h) I        */
@@ -143,6 +144,37 @@ SSD_API int ssd_abi_version(void);
  * SSD_ERR_TIMEOUT through ssd_check_device_status.  Process-wide; not for
  * production use.  Returns SSD_OK. */
 SSD_API int ssd_debug_set_wait(int64_t spin_limit, int64_t withhold_chunk);
+
+/* Allocation-free forward pass.  The paper has no counterpart to this entry
+ * point; it exists for callers that may not allocate device memory
+ * themselves: for example a plug-in inside a host application that owns the
+ * whole device-memory budget through its own pool, or a latency-bound loop
+ * in which cudaMalloc, which can synchronise the device, is not allowed.
+ *
+ * Same arguments and layouts as ssd_fwd, minus the workspace: it runs the
+ * generic path with its scratch in one fixed array of
+ * SSD_NOALLOC_SCRATCH_BYTES (64 MiB) compiled into the library.  Every GPU
+ * that loads the library holds that array until the process exits.  A
+ * problem whose scratch (256 B + 4*b*H*nc + 4*b*H*nc*N*P bytes, nc =
+ * ceil(T/Q)) does not fit is rejected with SSD_ERR_SCRATCH_LIMIT before
+ * anything is enqueued.  The function calls no cudaMalloc, cudaFree or other
+ * allocating routine.
+ *
+ * The first call on each device looks up that device's address of the array
+ * (with the device current); make that first call before any stream capture.
+ * All calls in the process share the one array and it keeps the previous
+ * call's contents (the status word is cleared by each call), so calls whose
+ * executions overlap on the GPU -- on different streams, or from different
+ * host threads without ordering -- race on it and give wrong results.
+ * The generic path has no device-side waits, so the return value (argument
+ * and launch errors) is the whole status of a call. */
+#define SSD_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+SSD_API int ssd_fwd_noalloc(const ssd_dims *dims,
+            const void *x, const float *dt, const float *A,
+            const void *B, const void *C, const float *D,
+            const float *init_state,
+            void *y, float *final_state,
+            void *stream);
 
 /* Measurement hook.  When both handles are non-NULL (cudaEvent_t values
  * created by the caller), every later ssd_fwd records `start_event` on its

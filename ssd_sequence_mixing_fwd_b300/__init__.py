@@ -28,6 +28,8 @@ SSD_ERR_WORKSPACE = 4
 SSD_ERR_CUDA = 5
 SSD_ERR_TIMEOUT = 6
 SSD_ERR_DEVICE = 7
+SSD_ERR_SCRATCH_LIMIT = 8
+SSD_NOALLOC_SCRATCH_BYTES = 64 << 20
 SSD_A_SCALAR = 0
 SSD_A_DIAGONAL = 1
 SSD_DTYPE_BF16 = 0
@@ -40,7 +42,7 @@ _PATHS = {"auto": SSD_PATH_AUTO, "generic": SSD_PATH_GENERIC, "tcgen05": SSD_PAT
 # Every symbol include/ssd.h declares.
 EXPORTED = ("ssd_fwd_workspace_size", "ssd_fwd_path", "ssd_fwd", "ssd_check_device_status",
             "ssd_status_string", "ssd_abi_version", "ssd_debug_set_wait",
-            "ssd_debug_set_kernel_events", "ssd_launch_count")
+            "ssd_debug_set_kernel_events", "ssd_launch_count", "ssd_fwd_noalloc")
 
 
 class ssd_dims(ctypes.Structure):
@@ -73,6 +75,7 @@ def load_library(path=LIB_PATH):
             lib.ssd_fwd_workspace_size.argtypes = [P_dims, ctypes.POINTER(sz)]
             lib.ssd_fwd_path.argtypes = [P_dims, ctypes.POINTER(ctypes.c_int32)]
             lib.ssd_fwd.argtypes = [P_dims] + [vp] * 9 + [vp, sz, vp]
+            lib.ssd_fwd_noalloc.argtypes = [P_dims] + [vp] * 9 + [vp]
             lib.ssd_check_device_status.argtypes = [vp, sz, vp]
             lib.ssd_status_string.argtypes = [ctypes.c_int]
             lib.ssd_status_string.restype = ctypes.c_char_p
@@ -82,7 +85,7 @@ def load_library(path=LIB_PATH):
             lib.ssd_launch_count.argtypes = [ctypes.POINTER(ctypes.c_uint64)]
             for name in ("ssd_fwd_workspace_size", "ssd_fwd_path", "ssd_fwd",
                          "ssd_check_device_status", "ssd_abi_version", "ssd_debug_set_wait",
-                         "ssd_debug_set_kernel_events", "ssd_launch_count"):
+                         "ssd_debug_set_kernel_events", "ssd_launch_count", "ssd_fwd_noalloc"):
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
     return _lib

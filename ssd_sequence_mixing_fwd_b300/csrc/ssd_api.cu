@@ -89,6 +89,8 @@ void record_dominant_stop(cudaStream_t s) {
     if (a && b) cudaEventRecord(static_cast<cudaEvent_t>(b), s);
 }
 
+int validate_dims(const ssd_dims *d, Problem *prob) { return check_dims(d, prob); }
+
 int64_t debug_spin_limit() { return g_spin_limit.load(); }
 int64_t debug_withhold_chunk() { return g_withhold.load(); }
 
@@ -108,6 +110,7 @@ extern "C" const char *ssd_status_string(int status) {
         case SSD_ERR_CUDA: return "CUDA error";
         case SSD_ERR_TIMEOUT: return "device wait timed out (outputs invalid)";
         case SSD_ERR_DEVICE: return "device-side check failed (outputs invalid)";
+        case SSD_ERR_SCRATCH_LIMIT: return "problem needs more scratch than the built-in array holds";
         default: return "unknown status";
     }
 }

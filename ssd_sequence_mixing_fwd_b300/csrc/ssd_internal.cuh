@@ -52,6 +52,8 @@ bool fused_supports(const Problem &p);
 cudaError_t fused_launch(const Problem &p, void *ws, size_t ws_bytes, cudaStream_t s);
 
 // ---- small helpers (csrc/ssd_api.cu) --------------------------------------
+// Host-side validation of ssd_dims shared by the entry points (fills *prob).
+int validate_dims(const ssd_dims *d, Problem *prob);
 // final_state <- init_state (or zero) for T == 0.
 cudaError_t launch_copy_state(const Problem &p, cudaStream_t s);
 
