@@ -343,9 +343,13 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's batch size (small cases for profiler captures)")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)        # at least 3 untimed warm-up steps
     w = WORKLOADS[args.workload]
+    if args.batch is not None:
+        w = w.with_(b=args.batch, name="%s_b%d" % (w.name, args.batch))
     out = run_reference(args, w) if args.impl == "reference" else run_ours(args, w)
     if out is not None:
         print(json.dumps(out), flush=True)

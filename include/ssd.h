@@ -93,7 +93,15 @@ typedef struct ssd_dims {
     int32_t reserved;  /* must be 0                                            */
 } ssd_dims;
 
-/* Bytes of device workspace ssd_fwd needs for `dims` (written to *bytes).
+/* Paths.  SSD_PATH_TCGEN05 (one fused persistent kernel: TMA loads, tcgen05
+ * tensor-core products with TMEM accumulators, block-to-block state hand-off
+ * through an L2-resident ring) takes scalar A, bf16 io, P == 64, N == 128 and
+ * Q in {128, 256}; it evaluates every chunk as 128-token blocks (for Q = 256,
+ * two blocks per chunk -- the chunked algorithm applied inside the chunk,
+ * equal up to rounding).  SSD_PATH_GENERIC (fp32 CUDA-core kernels) takes
+ * every dims the ABI accepts.  SSD_PATH_AUTO picks TCGEN05 where it applies.
+ *
+ * Bytes of device workspace ssd_fwd needs for `dims` (written to *bytes).
  * Host-only; enqueues nothing.  Returns SSD_ERR_INVALID_ARG /
  * SSD_ERR_UNSUPPORTED for dims ssd_fwd would reject. */
 SSD_API int ssd_fwd_workspace_size(const ssd_dims *dims, size_t *bytes);
@@ -138,11 +146,14 @@ SSD_API const char *ssd_status_string(int status);
 SSD_API int ssd_abi_version(void);
 
 /* Test hook for the failure-detection path of the fused kernel.
- * spin_limit: iteration limit of each inter-chunk wait (<= 0 restores the
- * default).  withhold_chunk: when >= 0, the work item of that chunk index
- * never publishes its state, so its successor's wait must run out and report
- * SSD_ERR_TIMEOUT through ssd_check_device_status.  Process-wide; not for
- * production use.  Returns SSD_OK. */
+ * The fused kernel hands the state from one 128-token block of a sequence to
+ * the next through global memory; each wait for it is bounded.
+ * spin_limit: iteration limit of each such wait (<= 0 restores the default).
+ * withhold_chunk: when >= 0, the work items of 128-token block number
+ * withhold_chunk never publish their state, so the next block's wait runs out,
+ * continues with a zero state, and the call reports SSD_ERR_TIMEOUT through
+ * ssd_check_device_status.  Process-wide; not for production use.
+ * Returns SSD_OK. */
 SSD_API int ssd_debug_set_wait(int64_t spin_limit, int64_t withhold_chunk);
 
 /* Allocation-free forward pass.  The paper has no counterpart to this entry
@@ -186,6 +197,11 @@ SSD_API int ssd_debug_set_kernel_events(void *start_event, void *stop_event);
 /* Number of kernels this process has launched through the library so far
  * (written to *count).  Host-side counter; returns SSD_OK. */
 SSD_API int ssd_launch_count(uint64_t *count);
+
+/* Text of the last CUDA runtime error a call of this library ran into (the
+ * cause behind the most recent SSD_ERR_CUDA), or "no error".  Process-wide,
+ * static storage, never NULL. */
+SSD_API const char *ssd_last_cuda_error(void);
 
 #ifdef __cplusplus
 }

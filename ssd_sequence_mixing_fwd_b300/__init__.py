@@ -42,7 +42,7 @@ _PATHS = {"auto": SSD_PATH_AUTO, "generic": SSD_PATH_GENERIC, "tcgen05": SSD_PAT
 # Every symbol include/ssd.h declares.
 EXPORTED = ("ssd_fwd_workspace_size", "ssd_fwd_path", "ssd_fwd", "ssd_check_device_status",
             "ssd_status_string", "ssd_abi_version", "ssd_debug_set_wait",
-            "ssd_debug_set_kernel_events", "ssd_launch_count", "ssd_fwd_noalloc")
+            "ssd_debug_set_kernel_events", "ssd_launch_count", "ssd_fwd_noalloc", "ssd_last_cuda_error")
 
 
 class ssd_dims(ctypes.Structure):
@@ -55,7 +55,10 @@ class ssd_dims(ctypes.Structure):
 class SSDError(RuntimeError):
     def __init__(self, status, what=""):
         self.status = status
-        super().__init__("%s: %s (status %d)" % (what or "ssd", ssd_status_string(status), status))
+        msg = "%s: %s (status %d)" % (what or "ssd", ssd_status_string(status), status)
+        if status == SSD_ERR_CUDA:
+            msg += ": " + ssd_last_cuda_error()
+        super().__init__(msg)
 
 
 _lib = None
@@ -79,6 +82,8 @@ def load_library(path=LIB_PATH):
             lib.ssd_check_device_status.argtypes = [vp, sz, vp]
             lib.ssd_status_string.argtypes = [ctypes.c_int]
             lib.ssd_status_string.restype = ctypes.c_char_p
+            lib.ssd_last_cuda_error.argtypes = []
+            lib.ssd_last_cuda_error.restype = ctypes.c_char_p
             lib.ssd_abi_version.argtypes = []
             lib.ssd_debug_set_wait.argtypes = [i64, i64]
             lib.ssd_debug_set_kernel_events.argtypes = [vp, vp]
@@ -96,6 +101,14 @@ def ssd_status_string(status):
         return load_library().ssd_status_string(int(status)).decode()
     except RuntimeError:
         return "status %d" % status
+
+
+def ssd_last_cuda_error():
+    """Text of the last CUDA error the library ran into."""
+    try:
+        return load_library().ssd_last_cuda_error().decode()
+    except RuntimeError:
+        return "library not loaded"
 
 
 def ssd_abi_version():

@@ -13,6 +13,7 @@ std::atomic<int64_t> g_withhold{-1};
 std::atomic<uint64_t> g_launches{0};
 std::atomic<void *> g_ev_start{nullptr};
 std::atomic<void *> g_ev_stop{nullptr};
+std::atomic<int> g_last_cuda{0};
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -80,6 +81,10 @@ cudaError_t launch_copy_state(const Problem &p, cudaStream_t s) {
 }
 
 void note_launches(int n) { g_launches.fetch_add((uint64_t)n); }
+int note_cuda(cudaError_t e) {
+    if (e != cudaSuccess) g_last_cuda.store((int)e);
+    return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
 void record_dominant_start(cudaStream_t s) {
     void *a = g_ev_start.load(), *b = g_ev_stop.load();
     if (a && b) cudaEventRecord(static_cast<cudaEvent_t>(a), s);
@@ -158,7 +163,7 @@ extern "C" int ssd_fwd(const ssd_dims *dims, const void *x, const float *dt, con
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
     cudaError_t e = cudaMemsetAsync(workspace, 0, kStatusBytes, s);
-    if (e != cudaSuccess) return SSD_ERR_CUDA;
+    if (e != cudaSuccess) return note_cuda(e);
     if (empty) {
         e = launch_copy_state(p, s);
     } else if (path == SSD_PATH_TCGEN05) {
@@ -166,17 +171,18 @@ extern "C" int ssd_fwd(const ssd_dims *dims, const void *x, const float *dt, con
     } else {
         e = generic_launch(p, generic_carve(p, workspace), s);
     }
-    return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+    return note_cuda(e);
 }
 
 extern "C" int ssd_check_device_status(void *workspace, size_t workspace_bytes, void *stream) {
     if (!workspace || workspace_bytes < sizeof(int)) return SSD_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (cudaStreamSynchronize(s) != cudaSuccess) return SSD_ERR_CUDA;
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return note_cuda(e);
     int word = 0;
-    if (cudaMemcpy(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return SSD_ERR_CUDA;
+    if ((e = cudaMemcpy(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess) return note_cuda(e);
     const int zero = 0;
-    if (cudaMemcpy(workspace, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return SSD_ERR_CUDA;
+    if ((e = cudaMemcpy(workspace, &zero, sizeof(int), cudaMemcpyHostToDevice)) != cudaSuccess) return note_cuda(e);
     return word;
 }
 
@@ -190,6 +196,10 @@ extern "C" int ssd_debug_set_kernel_events(void *start_event, void *stop_event) 
     g_ev_start.store(start_event);
     g_ev_stop.store(stop_event);
     return SSD_OK;
+}
+
+extern "C" const char *ssd_last_cuda_error(void) {
+    return cudaGetErrorString(static_cast<cudaError_t>(g_last_cuda.load()));
 }
 
 extern "C" int ssd_launch_count(uint64_t *count) {

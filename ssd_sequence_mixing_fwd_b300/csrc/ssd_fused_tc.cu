@@ -1,10 +1,932 @@
-// ssd_fused_tc.cu -- fused tcgen05/TMA path (not built yet: reports unsupported).
+// ssd_fused_tc.cu -- fused tcgen05/TMA path of the SSD chunked scan (sm_103a).
+//
+// One persistent kernel evaluates the whole forward pass (Structured State
+// Space Duality, "The chunked algorithm takes both"):
+//
+//   work item = (batch row, 128-token block, k heads of one B/C group)
+//     C_blk B_blk^T              once per item, tcgen05 -> TMEM (fp32)
+//     per head:
+//       cum_i                    prefix sums of dt*A over the block (fp32)
+//       S = C B^T o L            L_ij = exp(cum_i - cum_j), j <= i; fp16, kept in TMEM
+//       Y_diag = S X             tcgen05, A operand from TMEM
+//       s = B^T (w o X)          w_j = exp(cum_end - cum_j); the block's input projection
+//       h_prev                   state entering the block, from the previous block's item
+//       h = exp(cum_end) h_prev + s        fp32, published for the next block
+//       Y_off = C h_prev         tcgen05
+//       y = Y_diag + exp(cum_i) Y_off + D x
+//
+// A chunk of Q = 256 tokens is evaluated as two 128-token blocks: its diagonal
+// block is itself split by the chunked algorithm, whose result does not depend
+// on the block length ("exact, not an approximation"), so only rounding
+// differs from a single 256-token block.
+//
+// The serial part -- one state step per block -- runs through an fp32 ring of
+// two state slots per (batch, head) in global memory (L2 resident) with one
+// release/acquire flag per 32 state rows: the warp that owns rows n..n+31 of a
+// head publishes them and the same warp quarter of the next block's item
+// waits for exactly those rows.  Items are handed out in block-major order by
+// an atomic ticket, so every item that is waited on already runs on a
+// resident CTA.  Every wait is bounded: a chain wait that runs out records
+// SSD_ERR_TIMEOUT and continues with a zero state; an mbarrier wait that runs
+// out records SSD_ERR_TIMEOUT and the CTA winds down.
+//
+// Precision: C, B and X enter the tensor cores as fp16 (converted in shared
+// memory from bf16; exact in the normal range), the masked matrix S, w o X and
+// h_prev are rounded to fp16, all accumulation, decay sums and the state are
+// fp32 ("When it breaks").
+//
+// Warp roles (320 threads): warp 0 issues TMA loads and hands out items,
+// warp 1 owns TMEM and issues tcgen05.mma, warps 2-5 and 6-9 are two math
+// groups that take alternate heads (conversion, masks, state step, epilogue,
+// TMA stores of y).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <mutex>
+
 #include "ssd_internal.cuh"
 
 namespace ssd {
+namespace {
 
-bool fused_supports(const Problem &) { return false; }
-size_t fused_workspace_bytes(const Problem &) { return kStatusBytes; }
-cudaError_t fused_launch(const Problem &, void *, size_t, cudaStream_t) { return cudaErrorNotSupported; }
+constexpr int kBlk = 128;          // tokens per block = MMA M
+constexpr int kP = 64;             // head dim handled by this path
+constexpr int kN = 128;            // state dim handled by this path
+constexpr int kThreads = 320;
+constexpr int kMaxK = 8;           // heads per work item at most
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ---- shared memory map (offsets from a 1024-byte aligned base) -----------
+constexpr int kBox = kBlk * 64 * 2;                 // one 128 x 64 fp16 box: 16 KB
+constexpr int kStageBytes = 4 * kBox;               // C box0, C box1, B box0, B box1
+constexpr int kOffStage = 0;                        // 2 stages
+constexpr int kOffGroup = 2 * kStageBytes;          // per math group: X, W
+constexpr int kGroupBytes = 2 * kBox;
+constexpr int kOffCum = kOffGroup + 2 * kGroupBytes;        // float [2][128]
+constexpr int kOffV = kOffCum + 2 * 128 * 4;                // float [2][4][128]
+constexpr int kOffDt = kOffV + 2 * 4 * 128 * 4;             // float [2][4][128]
+constexpr int kOffTot = kOffDt + 2 * 4 * 128 * 4;           // float [2][4]
+constexpr int kOffItem = kOffTot + 2 * 4 * 4;               // int [2]
+constexpr int kOffMisc = kOffItem + 2 * 4;                  // tmem base, abort
+constexpr int kOffBar = ((kOffMisc + 16 + 7) / 8) * 8;      // mbarriers
+constexpr int kNumBars = 24;
+constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 1024;   // + alignment slack
+
+// mbarrier indices
+constexpr int B_CB_FULL = 0;        // [2] TMA landed C/B of a stage (+ item id)
+constexpr int B_CB_CONV = 2;        // [2] C/B converted to fp16 (the 4 warps of one group)
+constexpr int B_CB_EMPTY = 4;       // [2] all MMAs reading the stage are done
+constexpr int B_CBMMA_FULL = 6;     // C B^T of the current item is in TMEM
+constexpr int B_CBTMEM_EMPTY = 7;   // every mask of the item has read C B^T (8 warps)
+constexpr int B_X_FULL = 8;         // [2] TMA landed X of a head
+constexpr int B_X_EMPTY = 10;       // [2] y store has read the X buffer
+constexpr int B_XW_READY = 12;      // [2] X converted, w o X written (4 warps)
+constexpr int B_S_READY = 14;       // [2] S written to TMEM (4 warps)
+constexpr int B_ACC_FULL = 16;      // [2] Y_diag and s are in TMEM
+constexpr int B_HP_READY = 18;      // [2] h_prev (fp16) written, s read (4 warps)
+constexpr int B_YO_FULL = 20;       // [2] Y_off is in TMEM
+constexpr int B_TMEM_EMPTY = 22;    // [2] epilogue has read Y_diag / Y_off
+
+// TMEM columns (512 allocated)
+constexpr uint32_t kTmCB = 0;                       // 128 cols: C B^T (fp32)
+__host__ __device__ constexpr uint32_t tm_S(int g) { return 128 + 192 * g; }     // 64 cols fp16x2
+__host__ __device__ constexpr uint32_t tm_Yd(int g) { return 192 + 192 * g; }    // 64 cols
+__host__ __device__ constexpr uint32_t tm_Acc(int g) { return 256 + 192 * g; }   // 64 cols: s, then Y_off
+
+// Wait limits.  One try_wait suspends for at most about kSuspendNs, so an
+// mbarrier wait gives up after roughly kBarSpin * kSuspendNs (about 2 s); a
+// chain wait polls one L2 word per iteration (well under 1 us each).
+constexpr uint32_t kSuspendNs = 2000;
+constexpr uint32_t kBarSpin = 1u << 20;
+constexpr uint32_t kDrainSpin = 1u << 12;
+constexpr int64_t kDefaultChainSpin = int64_t(1) << 21;
+constexpr uint32_t kIdleSpin = 1u << 24;   // MMA event loop: passes without progress
+
+struct FusedParams {
+    const float *dt, *A, *D, *init;
+    float *final_state;
+    float *ring;          // (b*H, 2, N, P)
+    unsigned *flags;      // (b*H, 2, 4)
+    int *status;
+    unsigned *ticket;
+    int b, T, H, G, k, HG, nblk, total_items;
+    int64_t chain_spin;
+    int64_t withhold;
+};
+
+// ---- PTX wrappers ----------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(kSuspendNs)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void named_bar(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release(unsigned *p, unsigned v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1,
+                                            int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
+        "[%2];" ::"r"(dst),
+        "l"(map), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t src, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(map),
+                 "r"(src), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Shared-memory matrix descriptor, 128-byte swizzle (sm_100 descriptor version 1).
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+// Instruction descriptor of kind::f16: fp16 A and B, fp32 accumulator.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int a_mn, int b_mn) {
+    return (1u << 4) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+#define SSD_R8(o) "=r"(r[o]), "=r"(r[o + 1]), "=r"(r[o + 2]), "=r"(r[o + 3]), "=r"(r[o + 4]), "=r"(r[o + 5]), \
+                  "=r"(r[o + 6]), "=r"(r[o + 7])
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t *r = reinterpret_cast<uint32_t *>(v);
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : SSD_R8(0), SSD_R8(8), SSD_R8(16), SSD_R8(24)
+        : "r"(taddr));
+}
+#undef SSD_R8
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+    const uint32_t *r = reinterpret_cast<const uint32_t *>(v);
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+__device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+__device__ __forceinline__ float2 unpack_h2(uint32_t u) {
+    __half2 h = *reinterpret_cast<__half2 *>(&u);
+    return __half22float2(h);
+}
+__device__ __forceinline__ uint32_t bf2_to_h2(uint32_t u) {
+    __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162 *>(&u);
+    float2 f = __bfloat1622float2(b);
+    return pack_h2(f.x, f.y);
+}
+// Byte offset of 16-byte chunk c of row r in a 128-byte-row, 128B-swizzled tile.
+__device__ __forceinline__ uint32_t swz(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
+
+// ---- bounded waits -----------------------------------------------------------
+struct Ctl {
+    int *status;
+    volatile int *abort_flag;
+};
+__device__ __forceinline__ void set_status(int *status, int code) { atomicCAS(status, 0, code); }
+
+// Waits for `parity` of `bar`; false (and the CTA marked aborting) when the
+// iteration limit runs out or another thread of the CTA gave up already.
+__device__ __forceinline__ bool wait_bar(const Ctl &c, uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    for (uint32_t i = 0; i < kBarSpin; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255u) == 255u && *c.abort_flag) return false;
+    }
+    set_status(c.status, SSD_ERR_TIMEOUT);
+    *c.abort_flag = 1;
+    return false;
+}
+
+// Bounded wait that ignores the abort flag (used while winding down).
+__device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity) {
+    for (uint32_t i = 0; i < kDrainSpin; ++i)
+        if (mbar_try_wait(bar, parity)) return;
+}
+
+__device__ __forceinline__ void decode_item(const FusedParams &p, int t, int &bi, int &blk, int &hgi) {
+    const int per = p.b * p.HG;
+    blk = t / per;
+    const int rem = t - blk * per;
+    bi = rem / p.HG;
+    hgi = rem - bi * p.HG;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    ssd_fused_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_B,
+                     const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_y,
+                     const FusedParams p) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem =
+        reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    float *cumS = reinterpret_cast<float *>(smem + kOffCum);     // [2][128]
+    float *vS = reinterpret_cast<float *>(smem + kOffV);         // [2][4][128]
+    float *dtS = reinterpret_cast<float *>(smem + kOffDt);       // [2][4][128]
+    float *totS = reinterpret_cast<float *>(smem + kOffTot);     // [2][4]
+    int *itemS = reinterpret_cast<int *>(smem + kOffItem);       // [2]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
+    auto bar = [&](int i) -> uint32_t { return sbase + kOffBar + 8 * i; };
+    auto stage_c = [&](int st, int box) -> uint32_t { return sbase + kOffStage + st * kStageBytes + box * kBox; };
+    auto stage_b = [&](int st, int box) -> uint32_t {
+        return sbase + kOffStage + st * kStageBytes + (2 + box) * kBox;
+    };
+    auto grp_x = [&](int g) -> uint32_t { return sbase + kOffGroup + g * kGroupBytes; };
+    auto grp_w = [&](int g) -> uint32_t { return sbase + kOffGroup + g * kGroupBytes + kBox; };
+    const Ctl ctl{p.status, abort_flag};
+
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar(B_CB_FULL + s), 1);
+            mbar_init(bar(B_CB_CONV + s), 4);
+            mbar_init(bar(B_CB_EMPTY + s), 1);
+            mbar_init(bar(B_X_FULL + s), 1);
+            mbar_init(bar(B_X_EMPTY + s), 1);
+            mbar_init(bar(B_XW_READY + s), 4);
+            mbar_init(bar(B_S_READY + s), 4);
+            mbar_init(bar(B_ACC_FULL + s), 1);
+            mbar_init(bar(B_HP_READY + s), 4);
+            mbar_init(bar(B_YO_FULL + s), 1);
+            mbar_init(bar(B_TMEM_EMPTY + s), 1);
+        }
+        mbar_init(bar(B_CBMMA_FULL), 1);
+        mbar_init(bar(B_CBTMEM_EMPTY), 8);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(tmem_slot))
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int k = p.k;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int it = 0, flat = 0;
+            int xcnt[2] = {0, 0};
+            int last_cb_use[2] = {-1, -1};
+            bool ok = true;
+            for (;; ++it) {
+                const int st = it & 1;
+                if (it >= 2 && !(ok = wait_bar(ctl, bar(B_CB_EMPTY + st), ((it >> 1) - 1) & 1))) break;
+                const unsigned t = atomicAdd(p.ticket, 1u);
+                const int id = t < (unsigned)p.total_items ? (int)t : -1;
+                itemS[st] = id;
+                if (id < 0) {
+                    mbar_arrive(bar(B_CB_FULL + st));
+                    break;
+                }
+                int bi, blk, hgi;
+                decode_item(p, id, bi, blk, hgi);
+                const int t0 = blk * kBlk;
+                const int grp = (hgi * k) / (p.H / p.G);
+                mbar_expect_tx(bar(B_CB_FULL + st), kStageBytes);
+                last_cb_use[st] = it;
+                for (int bx = 0; bx < 2; ++bx) {
+                    tma_load_3d(stage_c(st, bx), &tm_C, bar(B_CB_FULL + st), grp * kN + 64 * bx, t0, bi);
+                    tma_load_3d(stage_b(st, bx), &tm_B, bar(B_CB_FULL + st), grp * kN + 64 * bx, t0, bi);
+                }
+                for (int j = 0; j < k; ++j, ++flat) {
+                    const int g = flat & 1;
+                    if (xcnt[g] >= 1 && !(ok = wait_bar(ctl, bar(B_X_EMPTY + g), (xcnt[g] - 1) & 1))) break;
+                    mbar_expect_tx(bar(B_X_FULL + g), kBox);
+                    tma_load_3d(grp_x(g), &tm_x, bar(B_X_FULL + g), (hgi * k + j) * kP, t0, bi);
+                    ++xcnt[g];
+                }
+                if (!ok) break;
+            }
+            // After an abort, wait (bounded) until every load issued has landed,
+            // so no copy writes shared memory after the CTA has gone.  In a normal
+            // finish every load has been consumed already.
+            if (!ok) {
+                for (int s = 0; s < 2; ++s) {
+                    if (last_cb_use[s] >= 0) drain_bar(bar(B_CB_FULL + s), (last_cb_use[s] >> 1) & 1);
+                    if (xcnt[s] >= 1) drain_bar(bar(B_X_FULL + s), (xcnt[s] - 1) & 1);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        // An event loop: C B^T of the next item, and for each math group the
+        // products of its next head -- s and Y_diag once X, w o X and S are ready,
+        // Y_off once h_prev is ready -- issued as soon as their inputs are, so that
+        // neither group waits on the other's progress.
+        if (lane == 0) {
+            const uint32_t id_cb = idesc_f16(128, 128, 0, 0);
+            const uint32_t id_st = idesc_f16(128, kP, 1, 1);
+            const uint32_t id_yd = idesc_f16(128, kP, 0, 1);
+            const uint32_t id_yo = idesc_f16(128, kP, 0, 1);
+            const bool has_d = p.D != nullptr;
+            int cb_it = 0;              // next item whose C B^T is to be issued
+            int end_it = INT32_MAX;     // index of the end-of-work item, once seen
+            int f[2] = {0, 1};          // next head (flat index) of each group
+            int ph[2] = {0, 0};         // 0: s and Y_diag next; 1: Y_off next
+            int n[2] = {0, 0};          // heads of each group completed
+            int yo_cnt[2] = {0, 0};     // Y_off issued for the item held in each stage
+            uint32_t idle = 0;
+            for (;;) {
+                bool progress = false;
+                if (cb_it < end_it) {
+                    const int st = cb_it & 1;
+                    const uint32_t par = (cb_it >> 1) & 1;
+                    if (mbar_test(bar(B_CB_FULL + st), par)) {
+                        if (itemS[st] < 0) {
+                            end_it = cb_it;
+                            progress = true;
+                        } else if (mbar_test(bar(B_CB_CONV + st), par) &&
+                                   (cb_it == 0 || mbar_test(bar(B_CBTMEM_EMPTY), (cb_it - 1) & 1))) {
+                            tc_fence_after();
+                            for (int kk = 0; kk < 8; ++kk) {
+                                const uint64_t a = sdesc(stage_c(st, kk >> 2) + 32 * (kk & 3), 16, 1024);
+                                const uint64_t b = sdesc(stage_b(st, kk >> 2) + 32 * (kk & 3), 16, 1024);
+                                mma_ss(tmem + kTmCB, a, b, id_cb, kk > 0);
+                            }
+                            mma_commit(bar(B_CBMMA_FULL));
+                            ++cb_it;
+                            progress = true;
+                        }
+                    }
+                }
+                bool busy = false;
+#pragma unroll
+                for (int g = 0; g < 2; ++g) {
+                    const int it = f[g] / k;
+                    if (it >= end_it) continue;
+                    busy = true;
+                    const int st = it & 1;
+                    if (ph[g] == 0) {
+                        if (it >= cb_it) continue;
+                        if (!mbar_test(bar(B_XW_READY + g), n[g] & 1)) continue;
+                        if (!mbar_test(bar(B_S_READY + g), n[g] & 1)) continue;
+                        if (n[g] >= 1 && !mbar_test(bar(B_TMEM_EMPTY + g), (n[g] - 1) & 1)) continue;
+                        tc_fence_after();
+                        // s = B^T (w o X): A = B^T (MN-major, two 64-row atoms), B = w o X (MN-major)
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint64_t a = sdesc(stage_b(st, 0) + 2048 * kk, kBox, 1024);
+                            const uint64_t b = sdesc(grp_w(g) + 2048 * kk, kBox, 1024);
+                            mma_ss(tmem + tm_Acc(g), a, b, id_st, kk > 0);
+                        }
+                        // Y_diag = S X: A = S from TMEM (fp16 pairs), B = X (MN-major)
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint64_t b = sdesc(grp_x(g) + 2048 * kk, kBox, 1024);
+                            mma_ts(tmem + tm_Yd(g), tmem + tm_S(g) + 8 * kk, b, id_yd, (kk > 0) || has_d);
+                        }
+                        mma_commit(bar(B_ACC_FULL + g));
+                        ph[g] = 1;
+                        progress = true;
+                    } else {
+                        if (!mbar_test(bar(B_HP_READY + g), n[g] & 1)) continue;
+                        tc_fence_after();
+                        // Y_off = C h_prev: A = C (K-major), B = h_prev (MN-major)
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint64_t a = sdesc(stage_c(st, kk >> 2) + 32 * (kk & 3), 16, 1024);
+                            const uint64_t b = sdesc(grp_w(g) + 2048 * kk, kBox, 1024);
+                            mma_ss(tmem + tm_Acc(g), a, b, id_yo, kk > 0);
+                        }
+                        mma_commit(bar(B_YO_FULL + g));
+                        if (++yo_cnt[st] == k) {
+                            yo_cnt[st] = 0;
+                            mma_commit(bar(B_CB_EMPTY + st));
+                        }
+                        ph[g] = 0;
+                        ++n[g];
+                        f[g] += 2;
+                        progress = true;
+                    }
+                }
+                if (!busy && cb_it >= end_it) break;
+                if (progress) {
+                    idle = 0;
+                } else if (++idle > kIdleSpin) {
+                    set_status(p.status, SSD_ERR_TIMEOUT);
+                    *abort_flag = 1;
+                    break;
+                } else if ((idle & 1023u) == 0 && *abort_flag) {
+                    break;
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ math groups
+        const int g = (warp - 2) >> 2;
+        const int q = warp & 3;                 // TMEM lane quarter
+        const int r = 32 * q + lane;            // row of this thread (token or state row)
+        const uint32_t lane_off = (uint32_t)(32 * q) << 16;
+        const int bar_id = 1 + g;
+        const bool leader = (warp == 2 + 4 * g) && lane == 0;
+        float *cum = cumS + 128 * g;
+        float *vq = vS + 512 * g;
+        float *tot = totS + 4 * g;
+        float *dts = dtS + 512 * g;             // [4][128]: dt of this group's heads in the item
+        unsigned char *xbuf = smem + kOffGroup + g * kGroupBytes;
+        unsigned char *wbuf = xbuf + kBox;
+        int it = 0, flat = 0, hcnt = 0;
+        bool ok = true;
+        for (;; ++it) {
+            const int st = it & 1;
+            if (!(ok = wait_bar(ctl, bar(B_CB_FULL + st), (it >> 1) & 1))) break;
+            const int id = itemS[st];
+            if (id < 0) break;
+            int bi, blk, hgi;
+            decode_item(p, id, bi, blk, hgi);
+            const int t0 = blk * kBlk;
+            const int L = min(kBlk, p.T - t0);
+            const int j0 = (g - flat) & 1;      // first head of this group in the item
+            // dt of this group's heads, all loads issued at once, kept in shared memory
+            {
+                float dv[kMaxK / 2];
+#pragma unroll
+                for (int s = 0; s < kMaxK / 2; ++s) {
+                    const int j = j0 + 2 * s;
+                    dv[s] = (j < k && r < L) ? p.dt[((int64_t)bi * p.T + t0 + r) * p.H + hgi * k + j] : 0.f;
+                }
+#pragma unroll
+                for (int s = 0; s < kMaxK / 2; ++s) dts[128 * s + r] = dv[s];
+            }
+            // C and B of this stage: bf16 -> fp16 in place, row r of all four boxes.  The
+            // group that owns the item's first head does it: that group has no Y_off
+            // of the previous item outstanding, so C B^T of this item never waits on
+            // the other group's state chain.
+            if (j0 == 0) {
+                unsigned char *base = smem + kOffStage + st * kStageBytes;
+#pragma unroll
+                for (int bx = 0; bx < 4; ++bx) {
+                    uint4 *row = reinterpret_cast<uint4 *>(base + bx * kBox + r * 128);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        uint4 u = row[c];
+                        u.x = bf2_to_h2(u.x);
+                        u.y = bf2_to_h2(u.y);
+                        u.z = bf2_to_h2(u.z);
+                        u.w = bf2_to_h2(u.w);
+                        row[c] = u;
+                    }
+                }
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_CB_CONV + st));
+            }
+            const int my_count = (k - j0 + 1) / 2;
+            if (my_count == 0 && lane == 0) mbar_arrive(bar(B_CBTMEM_EMPTY));
+            for (int s = 0; s < my_count && ok; ++s) {
+                const int j = j0 + 2 * s;
+                const int h = hgi * k + j;
+                const float Ah = p.A[h] * kLog2e;
+                // (1) cum (log2 units) over the block: warp scan, then across the group
+                float v = dts[128 * s + r] * Ah;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float u = __shfl_up_sync(0xffffffffu, v, o);
+                    if (lane >= o) v += u;
+                }
+                if (lane == 31) tot[q] = v;
+                // the previous head's y store must have read the W buffer before it is reused
+                if (leader) bulk_wait_read0();
+                named_bar(bar_id, 128);
+                float pre = 0.f, total = 0.f;
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq) {
+                    const float tq = tot[qq];
+                    pre += (qq < q) ? tq : 0.f;
+                    total += tq;
+                }
+                const float ci = pre + v;
+                cum[r] = ci;
+                named_bar(bar_id, 128);
+                // (2) X -> fp16 in place (for S X); w o X -> W; Y_diag <- D x (exact fp32, the
+                //     S X products accumulate onto it)
+                if (!(ok = wait_bar(ctl, bar(B_X_FULL + g), hcnt & 1))) break;
+                {
+                    const float w = ex2(total - ci);
+                    const float Dh = p.D ? p.D[h] : 0.f;
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        float dx[32];
+#pragma unroll
+                        for (int cc = 0; cc < 4; ++cc) {
+                            const int c = 4 * half + cc;
+                            const uint32_t off = swz(r, c);
+                            uint4 u = *reinterpret_cast<uint4 *>(xbuf + off);
+                            u.x = bf2_to_h2(u.x);
+                            u.y = bf2_to_h2(u.y);
+                            u.z = bf2_to_h2(u.z);
+                            u.w = bf2_to_h2(u.w);
+                            *reinterpret_cast<uint4 *>(xbuf + off) = u;
+                            const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+                            uint32_t ow[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 f2 = unpack_h2(uw[e]);
+                                ow[e] = pack_h2(f2.x * w, f2.y * w);
+                                dx[8 * cc + 2 * e] = Dh * f2.x;
+                                dx[8 * cc + 2 * e + 1] = Dh * f2.y;
+                            }
+                            *reinterpret_cast<uint4 *>(wbuf + off) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+                        }
+                        if (p.D) tmem_st32(tmem + lane_off + tm_Yd(g) + 32 * half, dx);
+                    }
+                    if (p.D) tmem_st_wait();
+                    fence_async_smem();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(B_XW_READY + g));
+                }
+                // (3) mask: S_ij = CB_ij * 2^(cum_i - cum_j), j <= i
+                //   column block J < q: rank-1 form u_i * v_j around R = cum at row 32q-1
+                //   J == q: direct; J > q: zero
+#pragma unroll
+                for (int qq = 1; qq < 4; ++qq)
+                    if (r < 32 * qq) vq[128 * qq + r] = ex2(cum[32 * qq - 1] - ci);
+                named_bar(bar_id, 128);
+                if (s == 0 && !(ok = wait_bar(ctl, bar(B_CBMMA_FULL), it & 1))) break;
+                tc_fence_after();
+                {
+                    const float u = (q > 0) ? ex2(ci - cum[32 * q - 1]) : 1.f;
+#pragma unroll
+                    for (int J = 0; J < 4; ++J) {
+                        uint32_t pk[16];
+                        if (J > q) {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) pk[e] = 0u;
+                        } else {
+                            float c[32];
+                            tmem_ld32(tmem + lane_off + kTmCB + 32 * J, c);
+                            tmem_ld_wait();
+                            if (J < q) {
+                                const float *vv = vq + 128 * q + 32 * J;
+#pragma unroll
+                                for (int e = 0; e < 32; e += 2)
+                                    pk[e >> 1] = pack_h2(c[e] * u * vv[e], c[e + 1] * u * vv[e + 1]);
+                            } else {
+                                const float *cj = cum + 32 * J;
+#pragma unroll
+                                for (int e = 0; e < 32; e += 2) {
+                                    const float m0 = (e <= lane) ? ex2(ci - cj[e]) : 0.f;
+                                    const float m1 = (e + 1 <= lane) ? ex2(ci - cj[e + 1]) : 0.f;
+                                    pk[e >> 1] = pack_h2(c[e] * m0, c[e + 1] * m1);
+                                }
+                            }
+                        }
+                        tmem_st16(tmem + lane_off + tm_S(g) + 16 * J, pk);
+                    }
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(bar(B_S_READY + g));
+                        if (s == my_count - 1) mbar_arrive(bar(B_CBTMEM_EMPTY));
+                    }
+                }
+                // (4) state step: h = 2^total h_prev + s; publish; h_prev (fp16) -> W buffer
+                if (!(ok = wait_bar(ctl, bar(B_ACC_FULL + g), hcnt & 1))) break;
+                tc_fence_after();
+                // S X has read the X buffer and x is in registers: it may be refilled.
+                if (leader) mbar_arrive(bar(B_X_EMPTY + g));
+                {
+                    const float a = ex2(total);
+                    const int64_t sidx = (int64_t)bi * p.H + h;
+                    const int nrow = r;
+                    const bool first = (blk == 0);
+                    const bool last = (blk == p.nblk - 1);
+                    // Ring slots are chunk-major -- float4 chunk e of state row n at
+                    // (e * 128 + n) -- so each warp-wide access is 512 contiguous bytes.
+                    // init_state / final_state keep the caller's (N, P) row-major layout.
+                    const float4 *src = nullptr;
+                    int src_stride = 1;                 // float4 step between chunks of a row
+                    if (first) {
+                        if (p.init) src = reinterpret_cast<const float4 *>(p.init + (sidx * kN + nrow) * kP);
+                    } else {
+                        const int ps = (blk - 1) & 1;
+                        const unsigned *fl = p.flags + (sidx * 2 + ps) * 4 + q;
+                        bool got = false;
+                        for (int64_t i = 0; i < p.chain_spin; ++i) {
+                            if (ld_acquire(fl) >= (unsigned)blk) {
+                                got = true;
+                                break;
+                            }
+                        }
+                        if (got) {
+                            src = reinterpret_cast<const float4 *>(p.ring + (sidx * 2 + ps) * kN * kP) + nrow;
+                            src_stride = kN;
+                        } else {
+                            set_status(p.status, SSD_ERR_TIMEOUT);
+                        }
+                    }
+                    float4 *dst = nullptr;
+                    int dst_stride = 1;
+                    if (last) {
+                        if (p.final_state) dst = reinterpret_cast<float4 *>(p.final_state + (sidx * kN + nrow) * kP);
+                    } else {
+                        dst = reinterpret_cast<float4 *>(p.ring + (sidx * 2 + (blk & 1)) * kN * kP) + nrow;
+                        dst_stride = kN;
+                    }
+                    float hp[64];
+                    if (src) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const float4 t4 = __ldcg(src + e * src_stride);
+                            hp[4 * e] = t4.x; hp[4 * e + 1] = t4.y; hp[4 * e + 2] = t4.z; hp[4 * e + 3] = t4.w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 64; ++e) hp[e] = 0.f;
+                    }
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        float sv[32];
+                        tmem_ld32(tmem + lane_off + tm_Acc(g) + 32 * half, sv);
+                        tmem_ld_wait();
+                        if (dst) {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                const int c0 = 32 * half + 4 * e;
+                                __stcg(dst + (8 * half + e) * dst_stride,
+                                       make_float4(fmaf(a, hp[c0], sv[4 * e]), fmaf(a, hp[c0 + 1], sv[4 * e + 1]),
+                                                   fmaf(a, hp[c0 + 2], sv[4 * e + 2]),
+                                                   fmaf(a, hp[c0 + 3], sv[4 * e + 3])));
+                            }
+                        }
+                    }
+                    if (!last) {
+                        fence_acq_rel_gpu();
+                        __syncwarp();
+                        if (lane == 0 && (int64_t)blk != p.withhold)
+                            st_release(p.flags + (sidx * 2 + (blk & 1)) * 4 + q, (unsigned)(blk + 1));
+                    }
+#pragma unroll
+                    for (int cc = 0; cc < 8; ++cc) {
+                        uint4 o;
+                        o.x = pack_h2(hp[8 * cc + 0], hp[8 * cc + 1]);
+                        o.y = pack_h2(hp[8 * cc + 2], hp[8 * cc + 3]);
+                        o.z = pack_h2(hp[8 * cc + 4], hp[8 * cc + 5]);
+                        o.w = pack_h2(hp[8 * cc + 6], hp[8 * cc + 7]);
+                        *reinterpret_cast<uint4 *>(wbuf + swz(nrow, cc)) = o;
+                    }
+                    fence_async_smem();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(B_HP_READY + g));
+                }
+                // (5) epilogue: y = Y_diag + 2^cum_i Y_off + D x  ->  bf16 into the W buffer, TMA store
+                if (!(ok = wait_bar(ctl, bar(B_YO_FULL + g), hcnt & 1))) break;
+                tc_fence_after();
+                {
+                    const float gi = ex2(ci);
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        float yd[32], yo[32];
+                        tmem_ld32(tmem + lane_off + tm_Yd(g) + 32 * half, yd);
+                        tmem_ld32(tmem + lane_off + tm_Acc(g) + 32 * half, yo);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int cc = 0; cc < 4; ++cc) {
+                            uint32_t ow[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int c0 = 8 * cc + 2 * e;
+                                ow[e] = pack_bf2(fmaf(gi, yo[c0], yd[c0]), fmaf(gi, yo[c0 + 1], yd[c0 + 1]));
+                            }
+                            *reinterpret_cast<uint4 *>(wbuf + swz(r, 4 * half + cc)) =
+                                make_uint4(ow[0], ow[1], ow[2], ow[3]);
+                        }
+                    }
+                    tc_fence_before();
+                    fence_async_smem();
+                    named_bar(bar_id, 128);
+                    if (leader) {
+                        mbar_arrive(bar(B_TMEM_EMPTY + g));
+                        tma_store_3d(&tm_y, grp_w(g), h * kP, t0, bi);
+                        bulk_commit();
+                    }
+                }
+                ++hcnt;
+            }
+            if (!ok) break;
+            flat += k;
+        }
+        if (leader) bulk_wait0();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");
+    }
+}
+
+// ---- host side ----------------------------------------------------------------
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    });
+    return fn;
+}
+
+// 3-D bf16 map over (inner, rows, batch) with a 64 x 128 box, 128-byte swizzle.
+bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows, uint64_t batch) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {inner, rows, batch};
+    cuuint64_t strides[2] = {inner * 2, inner * rows * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)kBlk, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int heads_per_item(const Problem &p) {
+    const int hpg = (int)(p.H / p.G);
+    int k = 1;
+    for (int c = 1; c <= kMaxK; ++c)
+        if (hpg % c == 0) k = c;
+    return k;
+}
+
+size_t flags_bytes(const Problem &p) { return align_up(sizeof(unsigned) * (size_t)(p.b * p.H * 2 * 4), 256); }
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+}  // namespace
+
+bool fused_supports(const Problem &p) {
+    if (p.a_mode != SSD_A_SCALAR || p.io_dtype != SSD_DTYPE_BF16) return false;
+    if (p.P != kP || p.N != kN) return false;
+    if (p.Q != 128 && p.Q != 256) return false;
+    if (p.T > (int64_t)INT32_MAX / 2 || p.b * p.H * 2 > (int64_t)INT32_MAX) return false;
+    const int64_t items = ((p.T + kBlk - 1) / kBlk) * p.b * (p.H / heads_per_item(p));
+    return items < (int64_t)INT32_MAX;
+}
+
+size_t fused_workspace_bytes(const Problem &p) {
+    return kStatusBytes + flags_bytes(p) + sizeof(float) * (size_t)(p.b * p.H * 2 * kN * kP);
+}
+
+cudaError_t fused_launch(const Problem &p, void *ws, size_t ws_bytes, cudaStream_t s) {
+    (void)ws_bytes;
+    char *base = static_cast<char *>(ws);
+    FusedParams fp;
+    fp.dt = p.dt;
+    fp.A = p.A;
+    fp.D = p.D;
+    fp.init = p.init;
+    fp.final_state = p.final_state;
+    fp.status = reinterpret_cast<int *>(base);
+    fp.ticket = reinterpret_cast<unsigned *>(base + 64);
+    fp.flags = reinterpret_cast<unsigned *>(base + kStatusBytes);
+    fp.ring = reinterpret_cast<float *>(base + kStatusBytes + flags_bytes(p));
+    fp.b = (int)p.b;
+    fp.T = (int)p.T;
+    fp.H = (int)p.H;
+    fp.G = (int)p.G;
+    fp.k = heads_per_item(p);
+    fp.HG = (int)(p.H / fp.k);
+    fp.nblk = (int)((p.T + kBlk - 1) / kBlk);
+    fp.total_items = fp.nblk * fp.b * fp.HG;
+    const int64_t spin = debug_spin_limit();
+    fp.chain_spin = spin > 0 ? spin : kDefaultChainSpin;
+    fp.withhold = debug_withhold_chunk();
+
+    CUtensorMap mx, mB, mC, my;
+    if (!make_map(&mx, p.x, (uint64_t)(p.H * p.P), (uint64_t)p.T, (uint64_t)p.b) ||
+        !make_map(&mB, p.B, (uint64_t)(p.G * p.N), (uint64_t)p.T, (uint64_t)p.b) ||
+        !make_map(&mC, p.C, (uint64_t)(p.G * p.N), (uint64_t)p.T, (uint64_t)p.b) ||
+        !make_map(&my, p.y, (uint64_t)(p.H * p.P), (uint64_t)p.T, (uint64_t)p.b))
+        return cudaErrorInvalidValue;
+
+    cudaError_t e = cudaMemsetAsync(ws, 0, kStatusBytes + flags_bytes(p), s);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(ssd_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int sms = sm_count();
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    const int grid = fp.total_items < sms ? fp.total_items : sms;
+    record_dominant_start(s);
+    ssd_fused_kernel<<<grid, kThreads, kSmemBytes, s>>>(mx, mB, mC, my, fp);
+    record_dominant_stop(s);
+    note_launches(1);
+    return cudaGetLastError();
+}
 
 }  // namespace ssd

@@ -64,6 +64,8 @@ int64_t debug_withhold_chunk();
 // Measurement hooks: count launches; bracket the dominant kernel with the
 // caller's events when set (ssd_debug_set_kernel_events).
 void note_launches(int n);
+// Records a failed CUDA call for ssd_last_cuda_error; returns SSD_OK or SSD_ERR_CUDA.
+int note_cuda(cudaError_t e);
 void record_dominant_start(cudaStream_t s);
 void record_dominant_stop(cudaStream_t s);
 

@@ -68,7 +68,7 @@ extern "C" int ssd_fwd_noalloc(const ssd_dims *dims, const void *x, const float 
     p.init = init_state; p.y = y; p.final_state = final_state;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaMemsetAsync(ws, 0, kStatusBytes, s);
-    if (e != cudaSuccess) return SSD_ERR_CUDA;
+    if (e != cudaSuccess) return note_cuda(e);
     e = empty ? launch_copy_state(p, s) : generic_launch(p, generic_carve(p, ws), s);
-    return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+    return note_cuda(e);
 }
