@@ -16,9 +16,9 @@
 //       y = Y_diag + exp(cum_i) Y_off + D x
 //
 // A chunk of Q = 256 tokens is evaluated as two 128-token blocks: its diagonal
-// block is itself split by the chunked algorithm, whose result does not depend
-// on the block length ("exact, not an approximation"), so only rounding
-// differs from a single 256-token block.
+// block is itself split by the chunked algorithm, whose result equals the
+// recurrence for any block length, so only rounding differs from a single
+// 256-token block.
 //
 // The serial part -- one state step per block -- runs through an fp32 ring of
 // two state slots per (batch, head) in global memory (L2 resident) with one
@@ -53,7 +53,7 @@ namespace {
 constexpr int kBlk = 128;          // tokens per block = MMA M
 constexpr int kP = 64;             // head dim handled by this path
 constexpr int kN = 128;            // state dim handled by this path
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;        // 12 warps: TMA, MMA, 2 x 4 math, 2 publishers
 constexpr int kMaxK = 8;           // heads per work item at most
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -69,8 +69,9 @@ constexpr int kOffDt = kOffV + 2 * 4 * 128 * 4;             // float [2][4][128]
 constexpr int kOffTot = kOffDt + 2 * 4 * 128 * 4;           // float [2][4]
 constexpr int kOffItem = kOffTot + 2 * 4 * 4;               // int [2]
 constexpr int kOffMisc = kOffItem + 2 * 4;                  // tmem base, abort
-constexpr int kOffBar = ((kOffMisc + 16 + 7) / 8) * 8;      // mbarriers
-constexpr int kNumBars = 24;
+constexpr int kOffPub = kOffMisc + 16;                      // int [2][2]: (stream, block) mailbox
+constexpr int kOffBar = ((kOffPub + 16 + 7) / 8) * 8;       // mbarriers
+constexpr int kNumBars = 28;
 constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 1024;   // + alignment slack
 
 // mbarrier indices
@@ -87,6 +88,8 @@ constexpr int B_ACC_FULL = 16;      // [2] Y_diag and s are in TMEM
 constexpr int B_HP_READY = 18;      // [2] h_prev (fp16) written, s read (4 warps)
 constexpr int B_YO_FULL = 20;       // [2] Y_off is in TMEM
 constexpr int B_TMEM_EMPTY = 22;    // [2] epilogue has read Y_diag / Y_off
+constexpr int B_PUB_FULL = 24;      // [2] a group stored a state: publish it (4 warps)
+constexpr int B_PUB_DONE = 26;      // [2] the publisher has taken the mailbox
 
 // TMEM columns (512 allocated)
 constexpr uint32_t kTmCB = 0;                       // 128 cols: C B^T (fp32)
@@ -166,6 +169,12 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
     unsigned v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
+}
+__device__ __forceinline__ void red_relaxed_add(unsigned *p, unsigned v) {
+    asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void red_release_add(unsigned *p, unsigned v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 __device__ __forceinline__ void st_release(unsigned *p, unsigned v) {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
@@ -322,6 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *dtS = reinterpret_cast<float *>(smem + kOffDt);       // [2][4][128]
     float *totS = reinterpret_cast<float *>(smem + kOffTot);     // [2][4]
     int *itemS = reinterpret_cast<int *>(smem + kOffItem);       // [2]
+    volatile int *pubS = reinterpret_cast<volatile int *>(smem + kOffPub);   // [2][2]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
     auto bar = [&](int i) -> uint32_t { return sbase + kOffBar + 8 * i; };
@@ -350,6 +360,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(bar(B_CBMMA_FULL), 1);
         mbar_init(bar(B_CBTMEM_EMPTY), 8);
+        for (int g2 = 0; g2 < 2; ++g2) {
+            mbar_init(bar(B_PUB_FULL + g2), 4);
+            mbar_init(bar(B_PUB_DONE + g2), 1);
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
@@ -424,9 +438,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             int cb_it = 0;              // next item whose C B^T is to be issued
             int end_it = INT32_MAX;     // index of the end-of-work item, once seen
             int f[2] = {0, 1};          // next head (flat index) of each group
-            int ph[2] = {0, 0};         // 0: s and Y_diag next; 1: Y_off next
+            int ph[2] = {0, 0};         // next product of each group: 0 s, 1 Y_diag, 2 Y_off
             int n[2] = {0, 0};          // heads of each group completed
-            int yo_cnt[2] = {0, 0};     // Y_off issued for the item held in each stage
+            int yo_cnt0 = 0, yo_cnt1 = 0;   // Y_off issued for the item held in stage 0 / 1
             uint32_t idle = 0;
             for (;;) {
                 bool progress = false;
@@ -459,37 +473,45 @@ __global__ void __launch_bounds__(kThreads, 1)
                     busy = true;
                     const int st = it & 1;
                     if (ph[g] == 0) {
+                        // s = B^T (w o X) as soon as w o X is in shared memory
                         if (it >= cb_it) continue;
                         if (!mbar_test(bar(B_XW_READY + g), n[g] & 1)) continue;
-                        if (!mbar_test(bar(B_S_READY + g), n[g] & 1)) continue;
                         if (n[g] >= 1 && !mbar_test(bar(B_TMEM_EMPTY + g), (n[g] - 1) & 1)) continue;
                         tc_fence_after();
-                        // s = B^T (w o X): A = B^T (MN-major, two 64-row atoms), B = w o X (MN-major)
+                        // A = B^T (MN-major, two 64-row atoms), B = w o X (MN-major)
                         for (int kk = 0; kk < 8; ++kk) {
                             const uint64_t a = sdesc(stage_b(st, 0) + 2048 * kk, kBox, 1024);
                             const uint64_t b = sdesc(grp_w(g) + 2048 * kk, kBox, 1024);
                             mma_ss(tmem + tm_Acc(g), a, b, id_st, kk > 0);
                         }
-                        // Y_diag = S X: A = S from TMEM (fp16 pairs), B = X (MN-major)
+                        mma_commit(bar(B_ACC_FULL + g));
+                        ph[g] = 1;
+                        progress = true;
+                    } else if (ph[g] == 1) {
+                        // Y_diag (+)= S X once S is in TMEM; its completion frees the X buffer
+                        if (!mbar_test(bar(B_S_READY + g), n[g] & 1)) continue;
+                        tc_fence_after();
                         for (int kk = 0; kk < 8; ++kk) {
                             const uint64_t b = sdesc(grp_x(g) + 2048 * kk, kBox, 1024);
                             mma_ts(tmem + tm_Yd(g), tmem + tm_S(g) + 8 * kk, b, id_yd, (kk > 0) || has_d);
                         }
-                        mma_commit(bar(B_ACC_FULL + g));
-                        ph[g] = 1;
+                        mma_commit(bar(B_X_EMPTY + g));
+                        ph[g] = 2;
                         progress = true;
                     } else {
+                        // Y_off = C h_prev once h_prev is in shared memory
                         if (!mbar_test(bar(B_HP_READY + g), n[g] & 1)) continue;
                         tc_fence_after();
-                        // Y_off = C h_prev: A = C (K-major), B = h_prev (MN-major)
                         for (int kk = 0; kk < 8; ++kk) {
                             const uint64_t a = sdesc(stage_c(st, kk >> 2) + 32 * (kk & 3), 16, 1024);
                             const uint64_t b = sdesc(grp_w(g) + 2048 * kk, kBox, 1024);
                             mma_ss(tmem + tm_Acc(g), a, b, id_yo, kk > 0);
                         }
                         mma_commit(bar(B_YO_FULL + g));
-                        if (++yo_cnt[st] == k) {
-                            yo_cnt[st] = 0;
+                        // after the item's last Y_off, the stage's C and B may be refilled
+                        int &yc = st ? yo_cnt1 : yo_cnt0;
+                        if (++yc == k) {
+                            yc = 0;
                             mma_commit(bar(B_CB_EMPTY + st));
                         }
                         ph[g] = 0;
@@ -510,6 +532,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
+    } else if (warp >= 10) {
+        // ------------------------------------------------------------ publishers
+        // One per math group: after the group's four warps have stored a block's
+        // state (mbarrier arrive = CTA-scope release), a GPU-scope fence makes
+        // those stores visible and the 32-row counters of the ring slot grow by 32.
+        const int g = warp - 10;
+        if (lane == 0) {
+            for (int m = 0;; ++m) {
+                if (!wait_bar(ctl, bar(B_PUB_FULL + g), m & 1)) break;
+                const int sidx = pubS[2 * g], blk = pubS[2 * g + 1];
+                if (sidx < 0) break;
+                fence_acq_rel_gpu();
+                unsigned *fl = p.flags + ((int64_t)sidx * 2 + (blk & 1)) * 4;
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq) red_relaxed_add(fl + qq, 32u);
+                mbar_arrive(bar(B_PUB_DONE + g));
+            }
+        }
     } else {
         // ------------------------------------------------------------ math groups
         const int g = (warp - 2) >> 2;
@@ -524,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float *dts = dtS + 512 * g;             // [4][128]: dt of this group's heads in the item
         unsigned char *xbuf = smem + kOffGroup + g * kGroupBytes;
         unsigned char *wbuf = xbuf + kBox;
-        int it = 0, flat = 0, hcnt = 0;
+        int it = 0, flat = 0, hcnt = 0, npub = 0;
         bool ok = true;
         for (;; ++it) {
             const int st = it & 1;
@@ -684,8 +724,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // (4) state step: h = 2^total h_prev + s; publish; h_prev (fp16) -> W buffer
                 if (!(ok = wait_bar(ctl, bar(B_ACC_FULL + g), hcnt & 1))) break;
                 tc_fence_after();
-                // S X has read the X buffer and x is in registers: it may be refilled.
-                if (leader) mbar_arrive(bar(B_X_EMPTY + g));
                 {
                     const float a = ex2(total);
                     const int64_t sidx = (int64_t)bi * p.H + h;
@@ -695,6 +733,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // Ring slots are chunk-major -- float4 chunk e of state row n at
                     // (e * 128 + n) -- so each warp-wide access is 512 contiguous bytes.
                     // init_state / final_state keep the caller's (N, P) row-major layout.
+                    // A slot's counter (one per 32 state rows) grows by 32 per publication,
+                    // one release add per row.
                     const float4 *src = nullptr;
                     int src_stride = 1;                 // float4 step between chunks of a row
                     if (first) {
@@ -702,9 +742,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     } else {
                         const int ps = (blk - 1) & 1;
                         const unsigned *fl = p.flags + (sidx * 2 + ps) * 4 + q;
+                        const unsigned want = 32u * (unsigned)((blk - 1) / 2 + 1);
                         bool got = false;
                         for (int64_t i = 0; i < p.chain_spin; ++i) {
-                            if (ld_acquire(fl) >= (unsigned)blk) {
+                            if (ld_acquire(fl) >= want) {
                                 got = true;
                                 break;
                             }
@@ -724,48 +765,52 @@ __global__ void __launch_bounds__(kThreads, 1)
                         dst = reinterpret_cast<float4 *>(p.ring + (sidx * 2 + (blk & 1)) * kN * kP) + nrow;
                         dst_stride = kN;
                     }
-                    float hp[64];
+                    float4 hp[16];
                     if (src) {
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const float4 t4 = __ldcg(src + e * src_stride);
-                            hp[4 * e] = t4.x; hp[4 * e + 1] = t4.y; hp[4 * e + 2] = t4.z; hp[4 * e + 3] = t4.w;
-                        }
+                        for (int e = 0; e < 16; ++e) hp[e] = __ldcg(src + e * src_stride);
                     } else {
 #pragma unroll
-                        for (int e = 0; e < 64; ++e) hp[e] = 0.f;
+                        for (int e = 0; e < 16; ++e) hp[e] = make_float4(0.f, 0.f, 0.f, 0.f);
                     }
+                    uint32_t hk[32];                    // h_prev as fp16 pairs, for C h_prev
+                    // s is read from TMEM while the global loads are in flight
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
                         float sv[32];
                         tmem_ld32(tmem + lane_off + tm_Acc(g) + 32 * half, sv);
                         tmem_ld_wait();
-                        if (dst) {
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                const int c0 = 32 * half + 4 * e;
-                                __stcg(dst + (8 * half + e) * dst_stride,
-                                       make_float4(fmaf(a, hp[c0], sv[4 * e]), fmaf(a, hp[c0 + 1], sv[4 * e + 1]),
-                                                   fmaf(a, hp[c0 + 2], sv[4 * e + 2]),
-                                                   fmaf(a, hp[c0 + 3], sv[4 * e + 3])));
-                            }
+                        for (int e8 = 0; e8 < 8; ++e8) {
+                            const int e = 8 * half + e8;
+                            const float4 t4 = hp[e];
+                            if (dst)
+                                __stcg(dst + e * dst_stride,
+                                       make_float4(fmaf(a, t4.x, sv[4 * e8]), fmaf(a, t4.y, sv[4 * e8 + 1]),
+                                                   fmaf(a, t4.z, sv[4 * e8 + 2]), fmaf(a, t4.w, sv[4 * e8 + 3])));
+                            hk[2 * e] = pack_h2(t4.x, t4.y);
+                            hk[2 * e + 1] = pack_h2(t4.z, t4.w);
                         }
                     }
-                    if (!last) {
-                        fence_acq_rel_gpu();
+                    if (!last && (int64_t)blk != p.withhold) {
+                        // Hand the publication to this group's publisher warp, which makes
+                        // the stores visible at GPU scope (fence) and bumps the counters,
+                        // so these warps do not wait for the fence.
+                        if (leader) {
+                            // (a wait that runs out has set the status; carrying on keeps the
+                            // group's named barriers in step)
+                            if (npub >= 1) wait_bar(ctl, bar(B_PUB_DONE + g), (npub - 1) & 1);
+                            pubS[2 * g] = (int)sidx;
+                            pubS[2 * g + 1] = blk;
+                        }
                         __syncwarp();
-                        if (lane == 0 && (int64_t)blk != p.withhold)
-                            st_release(p.flags + (sidx * 2 + (blk & 1)) * 4 + q, (unsigned)(blk + 1));
+                        if (lane == 0) mbar_arrive(bar(B_PUB_FULL + g));
+                        ++npub;
                     }
 #pragma unroll
-                    for (int cc = 0; cc < 8; ++cc) {
-                        uint4 o;
-                        o.x = pack_h2(hp[8 * cc + 0], hp[8 * cc + 1]);
-                        o.y = pack_h2(hp[8 * cc + 2], hp[8 * cc + 3]);
-                        o.z = pack_h2(hp[8 * cc + 4], hp[8 * cc + 5]);
-                        o.w = pack_h2(hp[8 * cc + 6], hp[8 * cc + 7]);
-                        *reinterpret_cast<uint4 *>(wbuf + swz(nrow, cc)) = o;
-                    }
+                    for (int cc = 0; cc < 8; ++cc)
+                        *reinterpret_cast<uint4 *>(wbuf + swz(nrow, cc)) =
+                            make_uint4(hk[4 * cc], hk[4 * cc + 1], hk[4 * cc + 2], hk[4 * cc + 3]);
                     fence_async_smem();
                     tc_fence_before();
                     __syncwarp();
@@ -809,6 +854,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             flat += k;
         }
         if (leader) bulk_wait0();
+        // tell the publisher there is nothing more to publish
+        if (leader) {
+            if (npub >= 1) wait_bar(ctl, bar(B_PUB_DONE + g), (npub - 1) & 1);
+            pubS[2 * g] = -1;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_PUB_FULL + g));
     }
 
     tc_fence_before();
