@@ -43,6 +43,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "ssd_internal.cuh"
@@ -65,13 +66,12 @@ constexpr int kOffGroup = 2 * kStageBytes;          // per math group: X, W
 constexpr int kGroupBytes = 2 * kBox;
 constexpr int kOffCum = kOffGroup + 2 * kGroupBytes;        // float [2][128]
 constexpr int kOffV = kOffCum + 2 * 128 * 4;                // float [2][4][128]
-constexpr int kOffDt = kOffV + 2 * 4 * 128 * 4;             // float [2][4][128]
-constexpr int kOffTot = kOffDt + 2 * 4 * 128 * 4;           // float [2][4]
-constexpr int kOffItem = kOffTot + 2 * 4 * 4;               // int [2]
+constexpr int kOffDt = kOffV + 2 * 4 * 128 * 4;             // float [2 stages][128][kMaxK]: dt tile
+constexpr int kOffItem = kOffDt + 2 * 128 * kMaxK * 4;      // int [2]
 constexpr int kOffMisc = kOffItem + 2 * 4;                  // tmem base, abort
 constexpr int kOffPub = kOffMisc + 16;                      // int [2][2]: (stream, block) mailbox
 constexpr int kOffBar = ((kOffPub + 16 + 7) / 8) * 8;       // mbarriers
-constexpr int kNumBars = 28;
+constexpr int kNumBars = 32;
 constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 1024;   // + alignment slack
 
 // mbarrier indices
@@ -90,6 +90,8 @@ constexpr int B_YO_FULL = 20;       // [2] Y_off is in TMEM
 constexpr int B_TMEM_EMPTY = 22;    // [2] epilogue has read Y_diag / Y_off
 constexpr int B_PUB_FULL = 24;      // [2] a group stored a state: publish it (4 warps)
 constexpr int B_PUB_DONE = 26;      // [2] the publisher has taken the mailbox
+constexpr int B_W_FREE = 28;        // [2] the previous y store has read the W buffer (leader)
+constexpr int B_Y_READY = 30;       // [2] all rows of y are in the W buffer (4 warps)
 
 // TMEM columns (512 allocated)
 constexpr uint32_t kTmCB = 0;                       // 128 cols: C B^T (fp32)
@@ -114,6 +116,7 @@ struct FusedParams {
     int *status;
     unsigned *ticket;
     int b, T, H, G, k, HG, nblk, total_items;
+    int dt_tma;           // dt tile comes by TMA (k and H multiples of 4), else by thread loads
     int64_t chain_spin;
     int64_t withhold;
 };
@@ -157,9 +160,6 @@ __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_re
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void named_bar(int id, int n) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -172,12 +172,6 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
 }
 __device__ __forceinline__ void red_relaxed_add(unsigned *p, unsigned v) {
     asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ void red_release_add(unsigned *p, unsigned v) {
-    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ void st_release(unsigned *p, unsigned v) {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1,
@@ -262,17 +256,35 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// Packed fp32 pairs (one instruction for two lanes of work).
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    float2 r;
+    asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "mul.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    float2 r;
+    asm("{\n\t.reg .b64 a, b, c, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "mov.b64 c, {%6, %7};\n\tfma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return r;
+}
+// bf16 pair -> fp32 pair (exact: bf16 is the top half of an fp32)
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t u) {
+    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
+}
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
     __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&h);
 }
+__device__ __forceinline__ uint32_t pack_h2f(float2 v) { return pack_h2(v.x, v.y); }
 __device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&h);
-}
-__device__ __forceinline__ float2 unpack_h2(uint32_t u) {
-    __half2 h = *reinterpret_cast<__half2 *>(&u);
-    return __half22float2(h);
 }
 __device__ __forceinline__ uint32_t bf2_to_h2(uint32_t u) {
     __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162 *>(&u);
@@ -319,7 +331,7 @@ __device__ __forceinline__ void decode_item(const FusedParams &p, int t, int &bi
 __global__ void __launch_bounds__(kThreads, 1)
     ssd_fused_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_B,
                      const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_y,
-                     const FusedParams p) {
+                     const __grid_constant__ CUtensorMap tm_dt, const FusedParams p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem =
         reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -328,8 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     float *cumS = reinterpret_cast<float *>(smem + kOffCum);     // [2][128]
     float *vS = reinterpret_cast<float *>(smem + kOffV);         // [2][4][128]
-    float *dtS = reinterpret_cast<float *>(smem + kOffDt);       // [2][4][128]
-    float *totS = reinterpret_cast<float *>(smem + kOffTot);     // [2][4]
+    float *dtT = reinterpret_cast<float *>(smem + kOffDt);       // [2][128][k]
     int *itemS = reinterpret_cast<int *>(smem + kOffItem);       // [2]
     volatile int *pubS = reinterpret_cast<volatile int *>(smem + kOffPub);   // [2][2]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
@@ -363,6 +374,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int g2 = 0; g2 < 2; ++g2) {
             mbar_init(bar(B_PUB_FULL + g2), 4);
             mbar_init(bar(B_PUB_DONE + g2), 1);
+            mbar_init(bar(B_W_FREE + g2), 1);
+            mbar_init(bar(B_Y_READY + g2), 4);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -398,8 +411,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 decode_item(p, id, bi, blk, hgi);
                 const int t0 = blk * kBlk;
                 const int grp = (hgi * k) / (p.H / p.G);
-                mbar_expect_tx(bar(B_CB_FULL + st), kStageBytes);
+                mbar_expect_tx(bar(B_CB_FULL + st), kStageBytes + (p.dt_tma ? kBlk * k * 4 : 0));
                 last_cb_use[st] = it;
+                if (p.dt_tma) tma_load_3d(sbase + kOffDt + st * (kBlk * kMaxK * 4), &tm_dt, bar(B_CB_FULL + st),
+                                          hgi * k, t0, bi);
                 for (int bx = 0; bx < 2; ++bx) {
                     tma_load_3d(stage_c(st, bx), &tm_C, bar(B_CB_FULL + st), grp * kN + 64 * bx, t0, bi);
                     tma_load_3d(stage_b(st, bx), &tm_B, bar(B_CB_FULL + st), grp * kN + 64 * bx, t0, bi);
@@ -454,10 +469,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         } else if (mbar_test(bar(B_CB_CONV + st), par) &&
                                    (cb_it == 0 || mbar_test(bar(B_CBTMEM_EMPTY), (cb_it - 1) & 1))) {
                             tc_fence_after();
+                            // K steps of 16: +32 bytes inside a swizzle atom, next atom = next box
+                            const uint64_t ca = sdesc(stage_c(st, 0), 16, 1024), cb = sdesc(stage_b(st, 0), 16, 1024);
                             for (int kk = 0; kk < 8; ++kk) {
-                                const uint64_t a = sdesc(stage_c(st, kk >> 2) + 32 * (kk & 3), 16, 1024);
-                                const uint64_t b = sdesc(stage_b(st, kk >> 2) + 32 * (kk & 3), 16, 1024);
-                                mma_ss(tmem + kTmCB, a, b, id_cb, kk > 0);
+                                const uint64_t o = (uint64_t)((kk >> 2) * (kBox >> 4) + 2 * (kk & 3));
+                                mma_ss(tmem + kTmCB, ca + o, cb + o, id_cb, kk > 0);
                             }
                             mma_commit(bar(B_CBMMA_FULL));
                             ++cb_it;
@@ -479,11 +495,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (n[g] >= 1 && !mbar_test(bar(B_TMEM_EMPTY + g), (n[g] - 1) & 1)) continue;
                         tc_fence_after();
                         // A = B^T (MN-major, two 64-row atoms), B = w o X (MN-major)
-                        for (int kk = 0; kk < 8; ++kk) {
-                            const uint64_t a = sdesc(stage_b(st, 0) + 2048 * kk, kBox, 1024);
-                            const uint64_t b = sdesc(grp_w(g) + 2048 * kk, kBox, 1024);
-                            mma_ss(tmem + tm_Acc(g), a, b, id_st, kk > 0);
-                        }
+                        const uint64_t da = sdesc(stage_b(st, 0), kBox, 1024), db = sdesc(grp_w(g), kBox, 1024);
+                        for (int kk = 0; kk < 8; ++kk)       // K steps of 16 rows: +2048 bytes
+                            mma_ss(tmem + tm_Acc(g), da + 128 * kk, db + 128 * kk, id_st, kk > 0);
                         mma_commit(bar(B_ACC_FULL + g));
                         ph[g] = 1;
                         progress = true;
@@ -491,10 +505,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // Y_diag (+)= S X once S is in TMEM; its completion frees the X buffer
                         if (!mbar_test(bar(B_S_READY + g), n[g] & 1)) continue;
                         tc_fence_after();
-                        for (int kk = 0; kk < 8; ++kk) {
-                            const uint64_t b = sdesc(grp_x(g) + 2048 * kk, kBox, 1024);
-                            mma_ts(tmem + tm_Yd(g), tmem + tm_S(g) + 8 * kk, b, id_yd, (kk > 0) || has_d);
-                        }
+                        const uint64_t dx = sdesc(grp_x(g), kBox, 1024);
+                        for (int kk = 0; kk < 8; ++kk)
+                            mma_ts(tmem + tm_Yd(g), tmem + tm_S(g) + 8 * kk, dx + 128 * kk, id_yd, (kk > 0) || has_d);
                         mma_commit(bar(B_X_EMPTY + g));
                         ph[g] = 2;
                         progress = true;
@@ -502,10 +515,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // Y_off = C h_prev once h_prev is in shared memory
                         if (!mbar_test(bar(B_HP_READY + g), n[g] & 1)) continue;
                         tc_fence_after();
+                        const uint64_t ca = sdesc(stage_c(st, 0), 16, 1024), db = sdesc(grp_w(g), kBox, 1024);
                         for (int kk = 0; kk < 8; ++kk) {
-                            const uint64_t a = sdesc(stage_c(st, kk >> 2) + 32 * (kk & 3), 16, 1024);
-                            const uint64_t b = sdesc(grp_w(g) + 2048 * kk, kBox, 1024);
-                            mma_ss(tmem + tm_Acc(g), a, b, id_yo, kk > 0);
+                            const uint64_t o = (uint64_t)((kk >> 2) * (kBox >> 4) + 2 * (kk & 3));
+                            mma_ss(tmem + tm_Acc(g), ca + o, db + 128 * kk, id_yo, kk > 0);
                         }
                         mma_commit(bar(B_YO_FULL + g));
                         // after the item's last Y_off, the stage's C and B may be refilled
@@ -556,14 +569,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = warp & 3;                 // TMEM lane quarter
         const int r = 32 * q + lane;            // row of this thread (token or state row)
         const uint32_t lane_off = (uint32_t)(32 * q) << 16;
-        const int bar_id = 1 + g;
         const bool leader = (warp == 2 + 4 * g) && lane == 0;
         float *cum = cumS + 128 * g;
         float *vq = vS + 512 * g;
-        float *tot = totS + 4 * g;
-        float *dts = dtS + 512 * g;             // [4][128]: dt of this group's heads in the item
         unsigned char *xbuf = smem + kOffGroup + g * kGroupBytes;
         unsigned char *wbuf = xbuf + kBox;
+        {
+            // the column blocks right of this quarter's diagonal block are zero in every S
+            uint32_t z[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) z[e] = 0u;
+#pragma unroll
+            for (int J = 1; J < 4; ++J)
+                if (J > q) tmem_st16(tmem + lane_off + tm_S(g) + 16 * J, z);
+            tmem_st_wait();
+        }
         int it = 0, flat = 0, hcnt = 0, npub = 0;
         bool ok = true;
         for (;; ++it) {
@@ -576,17 +596,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int t0 = blk * kBlk;
             const int L = min(kBlk, p.T - t0);
             const int j0 = (g - flat) & 1;      // first head of this group in the item
-            // dt of this group's heads, all loads issued at once, kept in shared memory
-            {
-                float dv[kMaxK / 2];
-#pragma unroll
-                for (int s = 0; s < kMaxK / 2; ++s) {
-                    const int j = j0 + 2 * s;
-                    dv[s] = (j < k && r < L) ? p.dt[((int64_t)bi * p.T + t0 + r) * p.H + hgi * k + j] : 0.f;
-                }
-#pragma unroll
-                for (int s = 0; s < kMaxK / 2; ++s) dts[128 * s + r] = dv[s];
-            }
             // C and B of this stage: bf16 -> fp16 in place, row r of all four boxes.  The
             // group that owns the item's first head does it: that group has no Y_off
             // of the previous item outstanding, so C B^T of this item never waits on
@@ -606,66 +615,90 @@ __global__ void __launch_bounds__(kThreads, 1)
                         row[c] = u;
                     }
                 }
+                if (!p.dt_tma) {
+                    // dt tile by thread loads (rows past the sequence end are zero)
+                    float *tile = dtT + st * (kBlk * kMaxK);
+                    for (int jj = 0; jj < k; ++jj)
+                        tile[r * k + jj] = (r < L) ? p.dt[((int64_t)bi * p.T + t0 + r) * p.H + hgi * k + jj] : 0.f;
+                }
                 fence_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(B_CB_CONV + st));
             }
+            // a thread-loaded dt tile is read (by every warp of both groups) only after all four
+            // warps of the converting group have written their rows
+            if (!p.dt_tma && !(ok = wait_bar(ctl, bar(B_CB_CONV + st), (it >> 1) & 1))) break;
+            const float *tile = dtT + st * (kBlk * kMaxK);
             const int my_count = (k - j0 + 1) / 2;
             if (my_count == 0 && lane == 0) mbar_arrive(bar(B_CBTMEM_EMPTY));
             for (int s = 0; s < my_count && ok; ++s) {
                 const int j = j0 + 2 * s;
                 const int h = hgi * k + j;
                 const float Ah = p.A[h] * kLog2e;
-                // (1) cum (log2 units) over the block: warp scan, then across the group
-                float v = dts[128 * s + r] * Ah;
+                // (1) cum (log2 units) over the block, per warp and without group barriers:
+                //     each warp scans the quarters up to its own (lane = row within a quarter),
+                //     keeps cum of its own rows (diagonal block) and the rank-1 factors
+                //     v_j = 2^(R - cum_j), R = cum at row 32q - 1, for the rows below.
+                float ci = 0.f, run = 0.f, Rq = 0.f;
+                float cm[3];
 #pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const float u = __shfl_up_sync(0xffffffffu, v, o);
-                    if (lane >= o) v += u;
-                }
-                if (lane == 31) tot[q] = v;
-                // the previous head's y store must have read the W buffer before it is reused
-                if (leader) bulk_wait_read0();
-                named_bar(bar_id, 128);
-                float pre = 0.f, total = 0.f;
+                for (int m = 0; m < 4; ++m) {
+                    float v = tile[(32 * m + lane) * k + j] * Ah;
 #pragma unroll
-                for (int qq = 0; qq < 4; ++qq) {
-                    const float tq = tot[qq];
-                    pre += (qq < q) ? tq : 0.f;
-                    total += tq;
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const float u2 = __shfl_up_sync(0xffffffffu, v, o);
+                        if (lane >= o) v += u2;
+                    }
+                    const float c_m = run + v;
+                    if (m < 3) cm[m] = c_m;
+                    if (m == q) {
+                        ci = c_m;
+                        Rq = run;
+                    }
+                    run += __shfl_sync(0xffffffffu, v, 31);
                 }
-                const float ci = pre + v;
-                cum[r] = ci;
-                named_bar(bar_id, 128);
+                const float total = run;
+                cum[r] = ci;                            // own rows only (diagonal block)
+#pragma unroll
+                for (int m = 0; m < 3; ++m)
+                    if (m < q) vq[128 * q + 32 * m + lane] = ex2(Rq - cm[m]);
+                __syncwarp();
                 // (2) X -> fp16 in place (for S X); w o X -> W; Y_diag <- D x (exact fp32, the
                 //     S X products accumulate onto it)
+                // the previous head's y store must have read the W buffer before it is reused
+                if (leader) {
+                    bulk_wait_read0();
+                    mbar_arrive(bar(B_W_FREE + g));
+                }
+                if (!(ok = wait_bar(ctl, bar(B_W_FREE + g), hcnt & 1))) break;
                 if (!(ok = wait_bar(ctl, bar(B_X_FULL + g), hcnt & 1))) break;
                 {
                     const float w = ex2(total - ci);
                     const float Dh = p.D ? p.D[h] : 0.f;
+                    const float2 w2 = make_float2(w, w), d2 = make_float2(Dh, Dh);
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
                         float dx[32];
+                        uint4 xin[4];
+#pragma unroll
+                        for (int cc = 0; cc < 4; ++cc)
+                            xin[cc] = *reinterpret_cast<const uint4 *>(xbuf + swz(r, 4 * half + cc));
 #pragma unroll
                         for (int cc = 0; cc < 4; ++cc) {
-                            const int c = 4 * half + cc;
-                            const uint32_t off = swz(r, c);
-                            uint4 u = *reinterpret_cast<uint4 *>(xbuf + off);
-                            u.x = bf2_to_h2(u.x);
-                            u.y = bf2_to_h2(u.y);
-                            u.z = bf2_to_h2(u.z);
-                            u.w = bf2_to_h2(u.w);
-                            *reinterpret_cast<uint4 *>(xbuf + off) = u;
-                            const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
-                            uint32_t ow[4];
+                            const uint32_t off = swz(r, 4 * half + cc);
+                            const uint32_t uw[4] = {xin[cc].x, xin[cc].y, xin[cc].z, xin[cc].w};
+                            uint32_t xo[4], wo[4];
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
-                                const float2 f2 = unpack_h2(uw[e]);
-                                ow[e] = pack_h2(f2.x * w, f2.y * w);
-                                dx[8 * cc + 2 * e] = Dh * f2.x;
-                                dx[8 * cc + 2 * e + 1] = Dh * f2.y;
+                                const float2 f = bf2_to_f2(uw[e]);
+                                xo[e] = pack_h2f(f);
+                                wo[e] = pack_h2f(mul2(f, w2));
+                                const float2 dv = mul2(f, d2);
+                                dx[8 * cc + 2 * e] = dv.x;
+                                dx[8 * cc + 2 * e + 1] = dv.y;
                             }
-                            *reinterpret_cast<uint4 *>(wbuf + off) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+                            *reinterpret_cast<uint4 *>(xbuf + off) = make_uint4(xo[0], xo[1], xo[2], xo[3]);
+                            *reinterpret_cast<uint4 *>(wbuf + off) = make_uint4(wo[0], wo[1], wo[2], wo[3]);
                         }
                         if (p.D) tmem_st32(tmem + lane_off + tm_Yd(g) + 32 * half, dx);
                     }
@@ -678,37 +711,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // (3) mask: S_ij = CB_ij * 2^(cum_i - cum_j), j <= i
                 //   column block J < q: rank-1 form u_i * v_j around R = cum at row 32q-1
                 //   J == q: direct; J > q: zero
-#pragma unroll
-                for (int qq = 1; qq < 4; ++qq)
-                    if (r < 32 * qq) vq[128 * qq + r] = ex2(cum[32 * qq - 1] - ci);
-                named_bar(bar_id, 128);
                 if (s == 0 && !(ok = wait_bar(ctl, bar(B_CBMMA_FULL), it & 1))) break;
                 tc_fence_after();
                 {
-                    const float u = (q > 0) ? ex2(ci - cum[32 * q - 1]) : 1.f;
+                    const float u = ex2(ci - Rq);
+                    const float2 u2 = make_float2(u, u);
+                    // column blocks J > q stay zero: written once per CTA before the loop
 #pragma unroll
                     for (int J = 0; J < 4; ++J) {
+                        if (J > q) continue;
                         uint32_t pk[16];
-                        if (J > q) {
+                        float c[32];
+                        tmem_ld32(tmem + lane_off + kTmCB + 32 * J, c);
+                        tmem_ld_wait();
+                        if (J < q) {
+                            const float2 *vv = reinterpret_cast<const float2 *>(vq + 128 * q + 32 * J);
 #pragma unroll
-                            for (int e = 0; e < 16; ++e) pk[e] = 0u;
+                            for (int e = 0; e < 16; ++e)
+                                pk[e] = pack_h2f(mul2(mul2(make_float2(c[2 * e], c[2 * e + 1]), u2), vv[e]));
                         } else {
-                            float c[32];
-                            tmem_ld32(tmem + lane_off + kTmCB + 32 * J, c);
-                            tmem_ld_wait();
-                            if (J < q) {
-                                const float *vv = vq + 128 * q + 32 * J;
+                            const float *cj = cum + 32 * J;
 #pragma unroll
-                                for (int e = 0; e < 32; e += 2)
-                                    pk[e >> 1] = pack_h2(c[e] * u * vv[e], c[e + 1] * u * vv[e + 1]);
-                            } else {
-                                const float *cj = cum + 32 * J;
-#pragma unroll
-                                for (int e = 0; e < 32; e += 2) {
-                                    const float m0 = (e <= lane) ? ex2(ci - cj[e]) : 0.f;
-                                    const float m1 = (e + 1 <= lane) ? ex2(ci - cj[e + 1]) : 0.f;
-                                    pk[e >> 1] = pack_h2(c[e] * m0, c[e + 1] * m1);
-                                }
+                            for (int e = 0; e < 32; e += 2) {
+                                const float m0 = (e <= lane) ? ex2(ci - cj[e]) : 0.f;
+                                const float m1 = (e + 1 <= lane) ? ex2(ci - cj[e + 1]) : 0.f;
+                                pk[e >> 1] = pack_h2f(mul2(make_float2(c[e], c[e + 1]), make_float2(m0, m1)));
                             }
                         }
                         tmem_st16(tmem + lane_off + tm_S(g) + 16 * J, pk);
@@ -726,6 +753,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 {
                     const float a = ex2(total);
+                    const float2 a2 = make_float2(a, a);
                     const int64_t sidx = (int64_t)bi * p.H + h;
                     const int nrow = r;
                     const bool first = (blk == 0);
@@ -784,10 +812,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int e8 = 0; e8 < 8; ++e8) {
                             const int e = 8 * half + e8;
                             const float4 t4 = hp[e];
-                            if (dst)
-                                __stcg(dst + e * dst_stride,
-                                       make_float4(fmaf(a, t4.x, sv[4 * e8]), fmaf(a, t4.y, sv[4 * e8 + 1]),
-                                                   fmaf(a, t4.z, sv[4 * e8 + 2]), fmaf(a, t4.w, sv[4 * e8 + 3])));
+                            if (dst) {
+                                const float2 lo = fma2(a2, make_float2(t4.x, t4.y), make_float2(sv[4 * e8], sv[4 * e8 + 1]));
+                                const float2 hi = fma2(a2, make_float2(t4.z, t4.w),
+                                                       make_float2(sv[4 * e8 + 2], sv[4 * e8 + 3]));
+                                __stcg(dst + e * dst_stride, make_float4(lo.x, lo.y, hi.x, hi.y));
+                            }
                             hk[2 * e] = pack_h2(t4.x, t4.y);
                             hk[2 * e + 1] = pack_h2(t4.z, t4.w);
                         }
@@ -821,6 +851,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 {
                     const float gi = ex2(ci);
+                    const float2 g2 = make_float2(gi, gi);
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
                         float yd[32], yo[32];
@@ -833,7 +864,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
                                 const int c0 = 8 * cc + 2 * e;
-                                ow[e] = pack_bf2(fmaf(gi, yo[c0], yd[c0]), fmaf(gi, yo[c0 + 1], yd[c0 + 1]));
+                                const float2 yv = fma2(g2, make_float2(yo[c0], yo[c0 + 1]),
+                                                       make_float2(yd[c0], yd[c0 + 1]));
+                                ow[e] = pack_bf2(yv.x, yv.y);
                             }
                             *reinterpret_cast<uint4 *>(wbuf + swz(r, 4 * half + cc)) =
                                 make_uint4(ow[0], ow[1], ow[2], ow[3]);
@@ -841,8 +874,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_before();
                     fence_async_smem();
-                    named_bar(bar_id, 128);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(B_Y_READY + g));
                     if (leader) {
+                        if (!wait_bar(ctl, bar(B_Y_READY + g), hcnt & 1)) ok = false;
+                        tc_fence_after();
                         mbar_arrive(bar(B_TMEM_EMPTY + g));
                         tma_store_3d(&tm_y, grp_w(g), h * kP, t0, bi);
                         bulk_commit();
@@ -891,6 +927,19 @@ EncodeTiledFn encode_fn() {
 }
 
 // 3-D bf16 map over (inner, rows, batch) with a 64 x 128 box, 128-byte swizzle.
+// 3-D fp32 map over dt (H, T, b) with a k x 128 box, no swizzle (k * 4 bytes a multiple of 16).
+bool make_dt_map(CUtensorMap *m, const float *dt, uint64_t H, uint64_t T, uint64_t b, uint32_t k) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {H, T, b};
+    cuuint64_t strides[2] = {H * 4, H * T * 4};
+    cuuint32_t box[3] = {k, (cuuint32_t)kBlk, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(dt), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows, uint64_t batch) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
@@ -960,7 +1009,11 @@ cudaError_t fused_launch(const Problem &p, void *ws, size_t ws_bytes, cudaStream
     fp.chain_spin = spin > 0 ? spin : kDefaultChainSpin;
     fp.withhold = debug_withhold_chunk();
 
-    CUtensorMap mx, mB, mC, my;
+    fp.dt_tma = (fp.k % 4 == 0 && p.H % 4 == 0) ? 1 : 0;
+    CUtensorMap mx, mB, mC, my, mdt;
+    std::memset(&mdt, 0, sizeof(mdt));
+    if (fp.dt_tma && !make_dt_map(&mdt, p.dt, (uint64_t)p.H, (uint64_t)p.T, (uint64_t)p.b, (uint32_t)fp.k))
+        return cudaErrorInvalidValue;
     if (!make_map(&mx, p.x, (uint64_t)(p.H * p.P), (uint64_t)p.T, (uint64_t)p.b) ||
         !make_map(&mB, p.B, (uint64_t)(p.G * p.N), (uint64_t)p.T, (uint64_t)p.b) ||
         !make_map(&mC, p.C, (uint64_t)(p.G * p.N), (uint64_t)p.T, (uint64_t)p.b) ||
@@ -975,7 +1028,7 @@ cudaError_t fused_launch(const Problem &p, void *ws, size_t ws_bytes, cudaStream
     if (sms <= 0) return cudaErrorInvalidDevice;
     const int grid = fp.total_items < sms ? fp.total_items : sms;
     record_dominant_start(s);
-    ssd_fused_kernel<<<grid, kThreads, kSmemBytes, s>>>(mx, mB, mC, my, fp);
+    ssd_fused_kernel<<<grid, kThreads, kSmemBytes, s>>>(mx, mB, mC, my, mdt, fp);
     record_dominant_stop(s);
     note_launches(1);
     return cudaGetLastError();
