@@ -35,10 +35,11 @@
 // h_prev are rounded to fp16, all accumulation, decay sums and the state are
 // fp32 ("When it breaks").
 //
-// Warp roles (320 threads): warp 0 issues TMA loads and hands out items,
-// warp 1 owns TMEM and issues tcgen05.mma, warps 2-5 and 6-9 are two math
-// groups that take alternate heads (conversion, masks, state step, epilogue,
-// TMA stores of y).
+// Warp roles (384 threads): warp 0 issues TMA loads and hands out items;
+// warp 1 owns TMEM and issues each item's C B^T; warps 2-5 and 6-9 are two
+// math groups that take alternate heads (conversion, masks, state step,
+// epilogue, TMA stores of y); warp 10 + g issues math group g's tcgen05.mma
+// products and publishes its states.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -77,7 +78,7 @@ constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 1024;   // + alignment slack
 // mbarrier indices
 constexpr int B_CB_FULL = 0;        // [2] TMA landed C/B of a stage (+ item id)
 constexpr int B_CB_CONV = 2;        // [2] C/B converted to fp16 (the 4 warps of one group)
-constexpr int B_CB_EMPTY = 4;       // [2] all MMAs reading the stage are done
+constexpr int B_CB_EMPTY = 4;       // [2] all MMAs reading the stage are done (one arrival per group)
 constexpr int B_CBMMA_FULL = 6;     // C B^T of the current item is in TMEM
 constexpr int B_CBTMEM_EMPTY = 7;   // every mask of the item has read C B^T (8 warps)
 constexpr int B_X_FULL = 8;         // [2] TMA landed X of a head
@@ -87,7 +88,8 @@ constexpr int B_S_READY = 14;       // [2] S written to TMEM (4 warps)
 constexpr int B_ACC_FULL = 16;      // [2] Y_diag and s are in TMEM
 constexpr int B_HP_READY = 18;      // [2] h_prev (fp16) written, s read (4 warps)
 constexpr int B_YO_FULL = 20;       // [2] Y_off is in TMEM
-constexpr int B_TMEM_EMPTY = 22;    // [2] epilogue has read Y_diag / Y_off
+// 22-23 unused: a head's XW_READY arrival follows each warp's epilogue of the
+// group's previous head, so it also says that head's TMEM columns are free
 constexpr int B_PUB_FULL = 24;      // [2] a group stored a state: publish it (4 warps)
 constexpr int B_PUB_DONE = 26;      // [2] the publisher has taken the mailbox
 constexpr int B_W_FREE = 28;        // [2] the previous y store has read the W buffer (leader)
@@ -359,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar(B_CB_FULL + s), 1);
             mbar_init(bar(B_CB_CONV + s), 4);
-            mbar_init(bar(B_CB_EMPTY + s), 1);
+            mbar_init(bar(B_CB_EMPTY + s), 2);
             mbar_init(bar(B_X_FULL + s), 1);
             mbar_init(bar(B_X_EMPTY + s), 1);
             mbar_init(bar(B_XW_READY + s), 4);
@@ -367,7 +369,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(B_ACC_FULL + s), 1);
             mbar_init(bar(B_HP_READY + s), 4);
             mbar_init(bar(B_YO_FULL + s), 1);
-            mbar_init(bar(B_TMEM_EMPTY + s), 1);
         }
         mbar_init(bar(B_CBMMA_FULL), 1);
         mbar_init(bar(B_CBTMEM_EMPTY), 8);
@@ -439,101 +440,100 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        // An event loop: C B^T of the next item, and for each math group the
-        // products of its next head -- s and Y_diag once X, w o X and S are ready,
-        // Y_off once h_prev is ready -- issued as soon as their inputs are, so that
-        // neither group waits on the other's progress.
+        // ------------------------------------------------------------ C B^T issuer
+        // Owns TMEM; issues each item's C B^T once its C and B are fp16 and every
+        // mask of the previous item has read the previous C B^T.
         if (lane == 0) {
             const uint32_t id_cb = idesc_f16(128, 128, 0, 0);
+            for (int it = 0;; ++it) {
+                const int st = it & 1;
+                const uint32_t par = (it >> 1) & 1;
+                if (!wait_bar(ctl, bar(B_CB_FULL + st), par)) break;
+                if (itemS[st] < 0) break;
+                if (!wait_bar(ctl, bar(B_CB_CONV + st), par)) break;
+                if (it >= 1 && !wait_bar(ctl, bar(B_CBTMEM_EMPTY), (it - 1) & 1)) break;
+                tc_fence_after();
+                // K steps of 16: +32 bytes inside a swizzle atom, next atom = next box
+                const uint64_t ca = sdesc(stage_c(st, 0), 16, 1024), cb = sdesc(stage_b(st, 0), 16, 1024);
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t o = (uint64_t)((kk >> 2) * (kBox >> 4) + 2 * (kk & 3));
+                    mma_ss(tmem + kTmCB, ca + o, cb + o, id_cb, kk > 0);
+                }
+                mma_commit(bar(B_CBMMA_FULL));
+            }
+        }
+    } else if (warp >= 10) {
+        // ------------------------------------------------------------ per-group issuer + publisher
+        // Warp 10 + g serves math group g only, so neither group's products wait behind
+        // the other's.  An event loop:
+        //  * publications: after the group's four warps have stored a block's state
+        //    (mbarrier arrive = CTA-scope release), a GPU-scope fence makes those stores
+        //    visible and the 32-row counters of the ring slot grow by 32;
+        //  * products of the group's current head, each as soon as its inputs are ready:
+        //    s = B^T (w o X), then Y_diag (+)= S X (its completion frees the X buffer),
+        //    then Y_off = C h_prev (after the item's last one, the stage's C/B are released).
+        const int g = warp - 10;
+        if (lane == 0) {
             const uint32_t id_st = idesc_f16(128, kP, 1, 1);
-            const uint32_t id_yd = idesc_f16(128, kP, 0, 1);
-            const uint32_t id_yo = idesc_f16(128, kP, 0, 1);
+            const uint32_t id_yx = idesc_f16(128, kP, 0, 1);
             const bool has_d = p.D != nullptr;
-            int cb_it = 0;              // next item whose C B^T is to be issued
-            int end_it = INT32_MAX;     // index of the end-of-work item, once seen
-            int f[2] = {0, 1};          // next head (flat index) of each group
-            int ph[2] = {0, 0};         // next product of each group: 0 s, 1 Y_diag, 2 Y_off
-            int n[2] = {0, 0};          // heads of each group completed
-            int yo_cnt0 = 0, yo_cnt1 = 0;   // Y_off issued for the item held in stage 0 / 1
+            int n = 0, ph = 0, m = 0;
+            int f = g, it = g / k, j = g - (g / k) * k;     // group g's n-th head is flat head 2n + g
             uint32_t idle = 0;
             for (;;) {
                 bool progress = false;
-                if (cb_it < end_it) {
-                    const int st = cb_it & 1;
-                    const uint32_t par = (cb_it >> 1) & 1;
-                    if (mbar_test(bar(B_CB_FULL + st), par)) {
-                        if (itemS[st] < 0) {
-                            end_it = cb_it;
-                            progress = true;
-                        } else if (mbar_test(bar(B_CB_CONV + st), par) &&
-                                   (cb_it == 0 || mbar_test(bar(B_CBTMEM_EMPTY), (cb_it - 1) & 1))) {
-                            tc_fence_after();
-                            // K steps of 16: +32 bytes inside a swizzle atom, next atom = next box
-                            const uint64_t ca = sdesc(stage_c(st, 0), 16, 1024), cb = sdesc(stage_b(st, 0), 16, 1024);
-                            for (int kk = 0; kk < 8; ++kk) {
-                                const uint64_t o = (uint64_t)((kk >> 2) * (kBox >> 4) + 2 * (kk & 3));
-                                mma_ss(tmem + kTmCB, ca + o, cb + o, id_cb, kk > 0);
-                            }
-                            mma_commit(bar(B_CBMMA_FULL));
-                            ++cb_it;
-                            progress = true;
-                        }
-                    }
-                }
-                bool busy = false;
-#pragma unroll
-                for (int g = 0; g < 2; ++g) {
-                    const int it = f[g] / k;
-                    if (it >= end_it) continue;
-                    busy = true;
-                    const int st = it & 1;
-                    if (ph[g] == 0) {
-                        // s = B^T (w o X) as soon as w o X is in shared memory
-                        if (it >= cb_it) continue;
-                        if (!mbar_test(bar(B_XW_READY + g), n[g] & 1)) continue;
-                        if (n[g] >= 1 && !mbar_test(bar(B_TMEM_EMPTY + g), (n[g] - 1) & 1)) continue;
+                const int st = it & 1;
+                if (ph == 0) {
+                    if (mbar_test(bar(B_XW_READY + g), n & 1) && mbar_test(bar(B_CB_CONV + st), (it >> 1) & 1)) {
                         tc_fence_after();
                         // A = B^T (MN-major, two 64-row atoms), B = w o X (MN-major)
                         const uint64_t da = sdesc(stage_b(st, 0), kBox, 1024), db = sdesc(grp_w(g), kBox, 1024);
                         for (int kk = 0; kk < 8; ++kk)       // K steps of 16 rows: +2048 bytes
                             mma_ss(tmem + tm_Acc(g), da + 128 * kk, db + 128 * kk, id_st, kk > 0);
                         mma_commit(bar(B_ACC_FULL + g));
-                        ph[g] = 1;
+                        ph = 1;
                         progress = true;
-                    } else if (ph[g] == 1) {
-                        // Y_diag (+)= S X once S is in TMEM; its completion frees the X buffer
-                        if (!mbar_test(bar(B_S_READY + g), n[g] & 1)) continue;
+                    }
+                } else if (ph == 1) {
+                    if (mbar_test(bar(B_S_READY + g), n & 1)) {
                         tc_fence_after();
                         const uint64_t dx = sdesc(grp_x(g), kBox, 1024);
                         for (int kk = 0; kk < 8; ++kk)
-                            mma_ts(tmem + tm_Yd(g), tmem + tm_S(g) + 8 * kk, dx + 128 * kk, id_yd, (kk > 0) || has_d);
+                            mma_ts(tmem + tm_Yd(g), tmem + tm_S(g) + 8 * kk, dx + 128 * kk, id_yx, (kk > 0) || has_d);
                         mma_commit(bar(B_X_EMPTY + g));
-                        ph[g] = 2;
+                        ph = 2;
                         progress = true;
-                    } else {
-                        // Y_off = C h_prev once h_prev is in shared memory
-                        if (!mbar_test(bar(B_HP_READY + g), n[g] & 1)) continue;
+                    }
+                } else {
+                    if (mbar_test(bar(B_HP_READY + g), n & 1)) {
                         tc_fence_after();
+                        // A = C (K-major), B = h_prev (MN-major)
                         const uint64_t ca = sdesc(stage_c(st, 0), 16, 1024), db = sdesc(grp_w(g), kBox, 1024);
                         for (int kk = 0; kk < 8; ++kk) {
                             const uint64_t o = (uint64_t)((kk >> 2) * (kBox >> 4) + 2 * (kk & 3));
-                            mma_ss(tmem + tm_Acc(g), ca + o, db + 128 * kk, id_yo, kk > 0);
+                            mma_ss(tmem + tm_Acc(g), ca + o, db + 128 * kk, id_yx, kk > 0);
                         }
                         mma_commit(bar(B_YO_FULL + g));
-                        // after the item's last Y_off, the stage's C and B may be refilled
-                        int &yc = st ? yo_cnt1 : yo_cnt0;
-                        if (++yc == k) {
-                            yc = 0;
-                            mma_commit(bar(B_CB_EMPTY + st));
-                        }
-                        ph[g] = 0;
-                        ++n[g];
-                        f[g] += 2;
+                        if (j + 2 >= k) mma_commit(bar(B_CB_EMPTY + st));   // the group's last head of the item
+                        ph = 0;
+                        ++n;
+                        f += 2;
+                        it = f / k;
+                        j = f - it * k;
                         progress = true;
                     }
                 }
-                if (!busy && cb_it >= end_it) break;
+                if (mbar_test(bar(B_PUB_FULL + g), m & 1)) {
+                    const int sidx = pubS[2 * g], blk = pubS[2 * g + 1];
+                    if (sidx < 0) break;            // the group has finished every head
+                    fence_acq_rel_gpu();
+                    unsigned *fl = p.flags + ((int64_t)sidx * 2 + (blk & 1)) * 4;
+#pragma unroll
+                    for (int qq = 0; qq < 4; ++qq) red_relaxed_add(fl + qq, 32u);
+                    mbar_arrive(bar(B_PUB_DONE + g));
+                    ++m;
+                    progress = true;
+                }
                 if (progress) {
                     idle = 0;
                 } else if (++idle > kIdleSpin) {
@@ -543,24 +543,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else if ((idle & 1023u) == 0 && *abort_flag) {
                     break;
                 }
-            }
-        }
-    } else if (warp >= 10) {
-        // ------------------------------------------------------------ publishers
-        // One per math group: after the group's four warps have stored a block's
-        // state (mbarrier arrive = CTA-scope release), a GPU-scope fence makes
-        // those stores visible and the 32-row counters of the ring slot grow by 32.
-        const int g = warp - 10;
-        if (lane == 0) {
-            for (int m = 0;; ++m) {
-                if (!wait_bar(ctl, bar(B_PUB_FULL + g), m & 1)) break;
-                const int sidx = pubS[2 * g], blk = pubS[2 * g + 1];
-                if (sidx < 0) break;
-                fence_acq_rel_gpu();
-                unsigned *fl = p.flags + ((int64_t)sidx * 2 + (blk & 1)) * 4;
-#pragma unroll
-                for (int qq = 0; qq < 4; ++qq) red_relaxed_add(fl + qq, 32u);
-                mbar_arrive(bar(B_PUB_DONE + g));
             }
         }
     } else {
@@ -630,7 +612,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!p.dt_tma && !(ok = wait_bar(ctl, bar(B_CB_CONV + st), (it >> 1) & 1))) break;
             const float *tile = dtT + st * (kBlk * kMaxK);
             const int my_count = (k - j0 + 1) / 2;
-            if (my_count == 0 && lane == 0) mbar_arrive(bar(B_CBTMEM_EMPTY));
+            if (my_count == 0) {
+                // no head of this item here: nothing of this group reads C B^T or the stage
+                if (lane == 0) mbar_arrive(bar(B_CBTMEM_EMPTY));
+                if (leader) mbar_arrive(bar(B_CB_EMPTY + st));
+            }
             for (int s = 0; s < my_count && ok; ++s) {
                 const int j = j0 + 2 * s;
                 const int h = hgi * k + j;
@@ -822,21 +808,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                             hk[2 * e + 1] = pack_h2(t4.z, t4.w);
                         }
                     }
-                    if (!last && (int64_t)blk != p.withhold) {
-                        // Hand the publication to this group's publisher warp, which makes
-                        // the stores visible at GPU scope (fence) and bumps the counters,
-                        // so these warps do not wait for the fence.
-                        if (leader) {
-                            // (a wait that runs out has set the status; carrying on keeps the
-                            // group's named barriers in step)
-                            if (npub >= 1) wait_bar(ctl, bar(B_PUB_DONE + g), (npub - 1) & 1);
-                            pubS[2 * g] = (int)sidx;
-                            pubS[2 * g + 1] = blk;
-                        }
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(bar(B_PUB_FULL + g));
-                        ++npub;
-                    }
 #pragma unroll
                     for (int cc = 0; cc < 8; ++cc)
                         *reinterpret_cast<uint4 *>(wbuf + swz(nrow, cc)) =
@@ -845,6 +816,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar(B_HP_READY + g));
+                    if (!last && (int64_t)blk != p.withhold) {
+                        // Hand the publication to this group's issuer warp, which makes the
+                        // stores visible at GPU scope (fence) and bumps the counters, so these
+                        // warps do not wait for the fence.  (h_prev is signalled first: the
+                        // issuer starts C h_prev before it fences.)
+                        if (leader) {
+                            // (a wait that runs out has set the status and the abort flag; the
+                            // other waits then end quickly)
+                            if (npub >= 1) wait_bar(ctl, bar(B_PUB_DONE + g), (npub - 1) & 1);
+                            pubS[2 * g] = (int)sidx;
+                            pubS[2 * g + 1] = blk;
+                        }
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar(B_PUB_FULL + g));
+                        ++npub;
+                    }
+
                 }
                 // (5) epilogue: y = Y_diag + 2^cum_i Y_off + D x  ->  bf16 into the W buffer, TMA store
                 if (!(ok = wait_bar(ctl, bar(B_YO_FULL + g), hcnt & 1))) break;
@@ -879,7 +867,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (leader) {
                         if (!wait_bar(ctl, bar(B_Y_READY + g), hcnt & 1)) ok = false;
                         tc_fence_after();
-                        mbar_arrive(bar(B_TMEM_EMPTY + g));
                         tma_store_3d(&tm_y, grp_w(g), h * kP, t0, bi);
                         bulk_commit();
                     }
