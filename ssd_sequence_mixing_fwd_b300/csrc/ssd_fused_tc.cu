@@ -71,7 +71,8 @@ constexpr int kOffDt = kOffV + 2 * 4 * 128 * 4;             // float [2 stages][
 constexpr int kOffItem = kOffDt + 2 * 128 * kMaxK * 4;      // int [2]
 constexpr int kOffMisc = kOffItem + 2 * 4;                  // tmem base, abort
 constexpr int kOffPub = kOffMisc + 16;                      // int [2][2]: (stream, block) mailbox
-constexpr int kOffBar = ((kOffPub + 16 + 7) / 8) * 8;       // mbarriers
+constexpr int kOffAD = kOffPub + 16;                        // float [8 warps][8]: A, D of the item's heads
+constexpr int kOffBar = ((kOffAD + 8 * 8 * 4 + 7) / 8) * 8;  // mbarriers
 constexpr int kNumBars = 32;
 constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 1024;   // + alignment slack
 
@@ -554,6 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool leader = (warp == 2 + 4 * g) && lane == 0;
         float *cum = cumS + 128 * g;
         float *vq = vS + 512 * g;
+        float *adw = reinterpret_cast<float *>(smem + kOffAD) + 8 * (warp - 2);
         unsigned char *xbuf = smem + kOffGroup + g * kGroupBytes;
         unsigned char *wbuf = xbuf + kBox;
         {
@@ -612,6 +614,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!p.dt_tma && !(ok = wait_bar(ctl, bar(B_CB_CONV + st), (it >> 1) & 1))) break;
             const float *tile = dtT + st * (kBlk * kMaxK);
             const int my_count = (k - j0 + 1) / 2;
+            // A (log2 units) and D of this group's heads in the item, one copy per warp
+            if (lane < my_count) {
+                const int hh = hgi * k + j0 + 2 * lane;
+                adw[2 * lane] = p.A[hh] * kLog2e;
+                adw[2 * lane + 1] = p.D ? p.D[hh] : 0.f;
+            }
+            __syncwarp();
             if (my_count == 0) {
                 // no head of this item here: nothing of this group reads C B^T or the stage
                 if (lane == 0) mbar_arrive(bar(B_CBTMEM_EMPTY));
@@ -620,28 +629,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < my_count && ok; ++s) {
                 const int j = j0 + 2 * s;
                 const int h = hgi * k + j;
-                const float Ah = p.A[h] * kLog2e;
+                const float Ah = adw[2 * s];
+                const float Dh = adw[2 * s + 1];
                 // (1) cum (log2 units) over the block, per warp and without group barriers:
                 //     each warp scans the quarters up to its own (lane = row within a quarter),
                 //     keeps cum of its own rows (diagonal block) and the rank-1 factors
                 //     v_j = 2^(R - cum_j), R = cum at row 32q - 1, for the rows below.
+                // the four quarter scans are independent until their offsets: interleaved
+                float vv4[4];
+#pragma unroll
+                for (int m = 0; m < 4; ++m) vv4[m] = tile[(32 * m + lane) * k + j] * Ah;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        const float u2 = __shfl_up_sync(0xffffffffu, vv4[m], o);
+                        if (lane >= o) vv4[m] += u2;
+                    }
+                }
+                float qs[4];
+#pragma unroll
+                for (int m = 0; m < 4; ++m) qs[m] = __shfl_sync(0xffffffffu, vv4[m], 31);
                 float ci = 0.f, run = 0.f, Rq = 0.f;
                 float cm[3];
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
-                    float v = tile[(32 * m + lane) * k + j] * Ah;
-#pragma unroll
-                    for (int o = 1; o < 32; o <<= 1) {
-                        const float u2 = __shfl_up_sync(0xffffffffu, v, o);
-                        if (lane >= o) v += u2;
-                    }
-                    const float c_m = run + v;
+                    const float c_m = run + vv4[m];
                     if (m < 3) cm[m] = c_m;
                     if (m == q) {
                         ci = c_m;
                         Rq = run;
                     }
-                    run += __shfl_sync(0xffffffffu, v, 31);
+                    run += qs[m];
                 }
                 const float total = run;
                 cum[r] = ci;                            // own rows only (diagonal block)
@@ -660,7 +679,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!(ok = wait_bar(ctl, bar(B_X_FULL + g), hcnt & 1))) break;
                 {
                     const float w = ex2(total - ci);
-                    const float Dh = p.D ? p.D[h] : 0.f;
                     const float2 w2 = make_float2(w, w), d2 = make_float2(Dh, Dh);
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
