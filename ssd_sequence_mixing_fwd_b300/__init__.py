@@ -167,14 +167,9 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def ssd_fwd(x, dt, A, B, C, D=None, init_state=None, chunk_Q=256, return_final_state=True,
-            path="auto", y=None, final_state=None, workspace=None, stream=None, check=False):
-    """SSD chunked-scan forward on the GPU.  Returns ``(y, final_state)``.
-
-    ``y``, ``final_state`` and ``workspace`` may be passed preallocated
-    (workspace: uint8 CUDA tensor of at least ``ssd_fwd_workspace_size``
-    bytes).  ``check=True`` synchronises and raises on a device-side error.
-    """
+def _marshal(x, dt, A, B, C, D, init_state, chunk_Q, return_final_state, path, y, final_state,
+             workspace, stream):
+    """Checks the tensors, allocates missing outputs, and builds the C ABI arguments."""
     import torch
     for name, t in (("x", x), ("dt", dt), ("A", A), ("B", B), ("C", C), ("D", D),
                     ("init_state", init_state)):
@@ -205,9 +200,22 @@ def ssd_fwd(x, dt, A, B, C, D=None, init_state=None, chunk_Q=256, return_final_s
     if workspace is None:
         workspace = torch.empty(max(ssd_fwd_workspace_size(dims), 256), device=dev, dtype=torch.uint8)
     s = torch.cuda.current_stream(dev) if stream is None else stream
-    st = load_library().ssd_fwd(ctypes.byref(dims), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C),
-                                _ptr(D), _ptr(init_state), _ptr(y), _ptr(final_state),
-                                _ptr(workspace), workspace.numel(), ctypes.c_void_p(s.cuda_stream))
+    args = (ctypes.byref(dims), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(init_state),
+            _ptr(y), _ptr(final_state), _ptr(workspace), workspace.numel(), ctypes.c_void_p(s.cuda_stream))
+    return dims, args, y, final_state, workspace, s
+
+
+def ssd_fwd(x, dt, A, B, C, D=None, init_state=None, chunk_Q=256, return_final_state=True,
+            path="auto", y=None, final_state=None, workspace=None, stream=None, check=False):
+    """SSD chunked-scan forward on the GPU.  Returns ``(y, final_state)``.
+
+    ``y``, ``final_state`` and ``workspace`` may be passed preallocated
+    (workspace: uint8 CUDA tensor of at least ``ssd_fwd_workspace_size``
+    bytes).  ``check=True`` synchronises and raises on a device-side error.
+    """
+    dims, args, y, final_state, workspace, s = _marshal(
+        x, dt, A, B, C, D, init_state, chunk_Q, return_final_state, path, y, final_state, workspace, stream)
+    st = load_library().ssd_fwd(*args)
     if st != SSD_OK:
         raise SSDError(st, "ssd_fwd")
     if check:
@@ -215,3 +223,37 @@ def ssd_fwd(x, dt, A, B, C, D=None, init_state=None, chunk_Q=256, return_final_s
         if st != SSD_OK:
             raise SSDError(st, "ssd_fwd (device)")
     return y, final_state
+
+
+class PreparedCall:
+    """One ssd_fwd call with its arguments checked and marshalled once.
+
+    For loops that run the same problem on the same buffers (serving steps,
+    benchmarks): each call of the object only crosses the C ABI, so the GPU
+    is not left idle while Python rebuilds arguments.  The tensors passed in
+    (and the outputs/workspace it allocates) must stay alive and in place;
+    their contents may change between calls.
+
+        run = PreparedCall(x, dt, A, B, C, D, chunk_Q=256)
+        y, final_state = run()
+    """
+
+    def __init__(self, x, dt, A, B, C, D=None, init_state=None, chunk_Q=256, return_final_state=True,
+                 path="auto", y=None, final_state=None, workspace=None, stream=None):
+        self._keep = (x, dt, A, B, C, D, init_state)
+        (self.dims, self._args, self.y, self.final_state, self.workspace,
+         self.stream) = _marshal(x, dt, A, B, C, D, init_state, chunk_Q, return_final_state, path, y,
+                                 final_state, workspace, stream)
+        self._fn = load_library().ssd_fwd
+
+    def __call__(self):
+        st = self._fn(*self._args)
+        if st != SSD_OK:
+            raise SSDError(st, "ssd_fwd")
+        return self.y, self.final_state
+
+    def check(self):
+        """Synchronise the stream and raise on a device-side error of the last call."""
+        st = ssd_check_device_status(self.workspace, self.stream)
+        if st != SSD_OK:
+            raise SSDError(st, "ssd_fwd (device)")

@@ -162,14 +162,12 @@ extern "C" int ssd_fwd(const ssd_dims *dims, const void *x, const float *dt, con
     p.init = init_state; p.y = y; p.final_state = final_state;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-    cudaError_t e = cudaMemsetAsync(workspace, 0, kStatusBytes, s);
-    if (e != cudaSuccess) return note_cuda(e);
-    if (empty) {
-        e = launch_copy_state(p, s);
-    } else if (path == SSD_PATH_TCGEN05) {
-        e = fused_launch(p, workspace, workspace_bytes, s);
+    cudaError_t e;
+    if (!empty && path == SSD_PATH_TCGEN05) {
+        e = fused_launch(p, workspace, workspace_bytes, s);   // clears its own status block and counters
     } else {
-        e = generic_launch(p, generic_carve(p, workspace), s);
+        e = cudaMemsetAsync(workspace, 0, kStatusBytes, s);
+        if (e == cudaSuccess) e = empty ? launch_copy_state(p, s) : generic_launch(p, generic_carve(p, workspace), s);
     }
     return note_cuda(e);
 }

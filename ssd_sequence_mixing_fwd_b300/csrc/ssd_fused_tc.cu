@@ -967,11 +967,25 @@ int heads_per_item(const Problem &p) {
 
 size_t flags_bytes(const Problem &p) { return align_up(sizeof(unsigned) * (size_t)(p.b * p.H * 2 * 4), 256); }
 
-int sm_count() {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    return n;
+// Per-device launch setup, done once per device: SM count and the kernel's
+// dynamic shared memory limit.  Returns the SM count (0 on failure).
+int device_setup() {
+    constexpr int kMaxDev = 64;
+    static int sms[kMaxDev] = {};
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
+    if (sms[dev] > 0) return sms[dev];
+    std::lock_guard<std::mutex> lock(mu);
+    if (sms[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        if (cudaFuncSetAttribute(ssd_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+            cudaSuccess)
+            return 0;
+        sms[dev] = n;
+    }
+    return sms[dev];
 }
 
 }  // namespace
@@ -1027,9 +1041,7 @@ cudaError_t fused_launch(const Problem &p, void *ws, size_t ws_bytes, cudaStream
 
     cudaError_t e = cudaMemsetAsync(ws, 0, kStatusBytes + flags_bytes(p), s);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(ssd_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    const int sms = sm_count();
+    const int sms = device_setup();
     if (sms <= 0) return cudaErrorInvalidDevice;
     const int grid = fp.total_items < sms ? fp.total_items : sms;
     record_dominant_start(s);

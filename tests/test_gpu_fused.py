@@ -101,3 +101,24 @@ def test_fused_repeated_calls_same_workspace(cuda_device):
         ys.append(y.clone())
     torch.cuda.synchronize()
     assert torch.equal(ys[0], ys[1]) and torch.equal(ys[1], ys[2])
+
+
+def test_prepared_call_matches_ssd_fwd(cuda_device):
+    """PreparedCall marshals once; after the inputs change in place it still computes the new result."""
+    w = Workload("t", b=2, T=512, H=8, P=64, N=128, G=1, Q=256, D="normal", seed=91)
+    inp = make_inputs(w)
+    d = _dev(inp, cuda_device)
+    run = ssd.PreparedCall(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], None, chunk_Q=w.Q)
+    y1, f1 = run()
+    run.check()
+    yr, fr = ssd.ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], None, chunk_Q=w.Q, check=True)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, yr) and torch.equal(f1, fr)
+    inp2 = make_inputs(w.with_(seed=92))
+    for k in ("x", "dt", "B", "C"):
+        d[k].copy_(inp2[k].to(cuda_device))
+    y2, f2 = run()
+    run.check()
+    yo, fo = oracle.recurrence(inp2["x"], inp2["dt"], inp["A"], inp2["B"], inp2["C"], inp["D"], None)
+    assert rel(y2.float().cpu().numpy(), yo) <= 2e-3
+    assert rel(f2.cpu().numpy(), fo) <= 2e-3
