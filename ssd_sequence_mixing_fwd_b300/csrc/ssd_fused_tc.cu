@@ -54,16 +54,17 @@ namespace {
 
 constexpr int kBlk = 128;          // tokens per block = MMA M
 constexpr int kP = 64;             // head dim handled by this path
-constexpr int kN = 128;            // state dim handled by this path
+constexpr int kN = 128;            // state rows per MMA tile; N = 128 * NS with NS = 1 or 2
 constexpr int kThreads = 384;        // 12 warps: TMA, MMA, 2 x 4 math, 2 publishers
 constexpr int kMaxK = 8;           // heads per work item at most
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---- shared memory map (offsets from a 1024-byte aligned base) -----------
 constexpr int kBox = kBlk * 64 * 2;                 // one 128 x 64 fp16 box: 16 KB
-constexpr int kStageBytes = 4 * kBox;               // C box0, C box1, B box0, B box1
+// A C/B stage holds 2 NS boxes of C then 2 NS boxes of B (NS = N / 128): 64 KB or 128 KB;
+// two stages for N = 128, one for N = 256 (128 KB either way).
 constexpr int kOffStage = 0;                        // 2 stages
-constexpr int kOffGroup = 2 * kStageBytes;          // per math group: X, W
+constexpr int kOffGroup = 8 * kBox;                 // per math group: X, W (N = 256: group 1's space holds h_prev)
 constexpr int kGroupBytes = 2 * kBox;
 constexpr int kOffCum = kOffGroup + 2 * kGroupBytes;        // float [2][128]
 constexpr int kOffV = kOffCum + 2 * 128 * 4;                // float [2][4][128]
@@ -71,8 +72,8 @@ constexpr int kOffDt = kOffV + 2 * 4 * 128 * 4;             // float [2 stages][
 constexpr int kOffItem = kOffDt + 2 * 128 * kMaxK * 4;      // int [2]
 constexpr int kOffMisc = kOffItem + 2 * 4;                  // tmem base, abort
 constexpr int kOffPub = kOffMisc + 16;                      // int [2][2]: (stream, block) mailbox
-constexpr int kOffAD = kOffPub + 16;                        // float [8 warps][8]: A, D of the item's heads
-constexpr int kOffBar = ((kOffAD + 8 * 8 * 4 + 7) / 8) * 8;  // mbarriers
+constexpr int kOffAD = kOffPub + 16;                        // float [8 warps][2 kMaxK]: A, D of the item's heads
+constexpr int kOffBar = ((kOffAD + 8 * 2 * kMaxK * 4 + 7) / 8) * 8;  // mbarriers
 constexpr int kNumBars = 32;
 constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 1024;   // + alignment slack
 
@@ -331,6 +332,7 @@ __device__ __forceinline__ void decode_item(const FusedParams &p, int t, int &bi
     hgi = rem - bi * p.HG;
 }
 
+template <int NS>
 __global__ void __launch_bounds__(kThreads, 1)
     ssd_fused_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_B,
                      const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_y,
@@ -340,6 +342,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // N = 128 NS state rows.  N = 128: two math groups, two C/B stages.  N = 256: one math
+    // group (its TMEM takes two 64-column state accumulators), one C/B stage, and the
+    // other group's buffers hold the 256 x 64 fp16 h_prev.
+    constexpr int kNr = kN * NS;
+    constexpr int NG = (NS == 1) ? 2 : 1;
+    constexpr int NST = (NS == 1) ? 2 : 1;
+    constexpr int kStage = 4 * NS * kBox;
 
     float *cumS = reinterpret_cast<float *>(smem + kOffCum);     // [2][128]
     float *vS = reinterpret_cast<float *>(smem + kOffV);         // [2][4][128]
@@ -349,12 +358,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
     auto bar = [&](int i) -> uint32_t { return sbase + kOffBar + 8 * i; };
-    auto stage_c = [&](int st, int box) -> uint32_t { return sbase + kOffStage + st * kStageBytes + box * kBox; };
+    auto stage_c = [&](int st, int box) -> uint32_t { return sbase + kOffStage + st * kStage + box * kBox; };
     auto stage_b = [&](int st, int box) -> uint32_t {
-        return sbase + kOffStage + st * kStageBytes + (2 + box) * kBox;
+        return sbase + kOffStage + st * kStage + (2 * NS + box) * kBox;
     };
     auto grp_x = [&](int g) -> uint32_t { return sbase + kOffGroup + g * kGroupBytes; };
     auto grp_w = [&](int g) -> uint32_t { return sbase + kOffGroup + g * kGroupBytes + kBox; };
+    // h_prev (fp16, N x 64, MN-major) for C h_prev: the W buffer, or 32 KB of spare buffers
+    auto grp_hp = [&](int g) -> uint32_t { return NS == 1 ? grp_w(g) : sbase + kOffGroup + kGroupBytes; };
     const Ctl ctl{p.status, abort_flag};
 
     if (threadIdx.x == 0) {
@@ -362,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar(B_CB_FULL + s), 1);
             mbar_init(bar(B_CB_CONV + s), 4);
-            mbar_init(bar(B_CB_EMPTY + s), 2);
+            mbar_init(bar(B_CB_EMPTY + s), NG);
             mbar_init(bar(B_X_FULL + s), 1);
             mbar_init(bar(B_X_EMPTY + s), 1);
             mbar_init(bar(B_XW_READY + s), 4);
@@ -372,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(B_YO_FULL + s), 1);
         }
         mbar_init(bar(B_CBMMA_FULL), 1);
-        mbar_init(bar(B_CBTMEM_EMPTY), 8);
+        mbar_init(bar(B_CBTMEM_EMPTY), 4 * NG);
         for (int g2 = 0; g2 < 2; ++g2) {
             mbar_init(bar(B_PUB_FULL + g2), 4);
             mbar_init(bar(B_PUB_DONE + g2), 1);
@@ -400,8 +411,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             int last_cb_use[2] = {-1, -1};
             bool ok = true;
             for (;; ++it) {
-                const int st = it & 1;
-                if (it >= 2 && !(ok = wait_bar(ctl, bar(B_CB_EMPTY + st), ((it >> 1) - 1) & 1))) break;
+                const int st = it % NST;
+                if (it >= NST && !(ok = wait_bar(ctl, bar(B_CB_EMPTY + st), ((it / NST) - 1) & 1))) break;
                 const unsigned t = atomicAdd(p.ticket, 1u);
                 const int id = t < (unsigned)p.total_items ? (int)t : -1;
                 itemS[st] = id;
@@ -413,16 +424,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 decode_item(p, id, bi, blk, hgi);
                 const int t0 = blk * kBlk;
                 const int grp = (hgi * k) / (p.H / p.G);
-                mbar_expect_tx(bar(B_CB_FULL + st), kStageBytes + (p.dt_tma ? kBlk * k * 4 : 0));
+                mbar_expect_tx(bar(B_CB_FULL + st), kStage + (p.dt_tma ? kBlk * k * 4 : 0));
                 last_cb_use[st] = it;
                 if (p.dt_tma) tma_load_3d(sbase + kOffDt + st * (kBlk * kMaxK * 4), &tm_dt, bar(B_CB_FULL + st),
                                           hgi * k, t0, bi);
-                for (int bx = 0; bx < 2; ++bx) {
-                    tma_load_3d(stage_c(st, bx), &tm_C, bar(B_CB_FULL + st), grp * kN + 64 * bx, t0, bi);
-                    tma_load_3d(stage_b(st, bx), &tm_B, bar(B_CB_FULL + st), grp * kN + 64 * bx, t0, bi);
+                for (int bx = 0; bx < 2 * NS; ++bx) {
+                    tma_load_3d(stage_c(st, bx), &tm_C, bar(B_CB_FULL + st), grp * kNr + 64 * bx, t0, bi);
+                    tma_load_3d(stage_b(st, bx), &tm_B, bar(B_CB_FULL + st), grp * kNr + 64 * bx, t0, bi);
                 }
                 for (int j = 0; j < k; ++j, ++flat) {
-                    const int g = flat & 1;
+                    const int g = flat % NG;
                     if (xcnt[g] >= 1 && !(ok = wait_bar(ctl, bar(B_X_EMPTY + g), (xcnt[g] - 1) & 1))) break;
                     mbar_expect_tx(bar(B_X_FULL + g), kBox);
                     tma_load_3d(grp_x(g), &tm_x, bar(B_X_FULL + g), (hgi * k + j) * kP, t0, bi);
@@ -435,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // finish every load has been consumed already.
             if (!ok) {
                 for (int s = 0; s < 2; ++s) {
-                    if (last_cb_use[s] >= 0) drain_bar(bar(B_CB_FULL + s), (last_cb_use[s] >> 1) & 1);
+                    if (last_cb_use[s] >= 0) drain_bar(bar(B_CB_FULL + s), (last_cb_use[s] / NST) & 1);
                     if (xcnt[s] >= 1) drain_bar(bar(B_X_FULL + s), (xcnt[s] - 1) & 1);
                 }
             }
@@ -447,8 +458,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             const uint32_t id_cb = idesc_f16(128, 128, 0, 0);
             for (int it = 0;; ++it) {
-                const int st = it & 1;
-                const uint32_t par = (it >> 1) & 1;
+                const int st = it % NST;
+                const uint32_t par = (it / NST) & 1;
                 if (!wait_bar(ctl, bar(B_CB_FULL + st), par)) break;
                 if (itemS[st] < 0) break;
                 if (!wait_bar(ctl, bar(B_CB_CONV + st), par)) break;
@@ -456,14 +467,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 // K steps of 16: +32 bytes inside a swizzle atom, next atom = next box
                 const uint64_t ca = sdesc(stage_c(st, 0), 16, 1024), cb = sdesc(stage_b(st, 0), 16, 1024);
-                for (int kk = 0; kk < 8; ++kk) {
+                for (int kk = 0; kk < 8 * NS; ++kk) {
                     const uint64_t o = (uint64_t)((kk >> 2) * (kBox >> 4) + 2 * (kk & 3));
                     mma_ss(tmem + kTmCB, ca + o, cb + o, id_cb, kk > 0);
                 }
                 mma_commit(bar(B_CBMMA_FULL));
             }
         }
-    } else if (warp >= 10) {
+    } else if (warp >= 10 && warp < 10 + NG) {
         // ------------------------------------------------------------ per-group issuer + publisher
         // Warp 10 + g serves math group g only, so neither group's products wait behind
         // the other's.  An event loop:
@@ -479,18 +490,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t id_yx = idesc_f16(128, kP, 0, 1);
             const bool has_d = p.D != nullptr;
             int n = 0, ph = 0, m = 0;
-            int f = g, it = g / k, j = g - (g / k) * k;     // group g's n-th head is flat head 2n + g
+            int f = g, it = g / k, j = g - (g / k) * k;     // group g's n-th head is flat head NG n + g
             uint32_t idle = 0;
             for (;;) {
                 bool progress = false;
-                const int st = it & 1;
+                const int st = it % NST;
                 if (ph == 0) {
-                    if (mbar_test(bar(B_XW_READY + g), n & 1) && mbar_test(bar(B_CB_CONV + st), (it >> 1) & 1)) {
+                    if (mbar_test(bar(B_XW_READY + g), n & 1) && mbar_test(bar(B_CB_CONV + st), (it / NST) & 1)) {
                         tc_fence_after();
                         // A = B^T (MN-major, two 64-row atoms), B = w o X (MN-major)
-                        const uint64_t da = sdesc(stage_b(st, 0), kBox, 1024), db = sdesc(grp_w(g), kBox, 1024);
-                        for (int kk = 0; kk < 8; ++kk)       // K steps of 16 rows: +2048 bytes
-                            mma_ss(tmem + tm_Acc(g), da + 128 * kk, db + 128 * kk, id_st, kk > 0);
+                        // one M = 128 product per 128 state rows (A = two 64-row atoms of B each)
+                        const uint64_t db = sdesc(grp_w(g), kBox, 1024);
+#pragma unroll
+                        for (int hf = 0; hf < NS; ++hf) {
+                            const uint64_t da = sdesc(stage_b(st, 2 * hf), kBox, 1024);
+                            for (int kk = 0; kk < 8; ++kk)   // K steps of 16 rows: +2048 bytes
+                                mma_ss(tmem + tm_Acc(g) + 64 * hf, da + 128 * kk, db + 128 * kk, id_st, kk > 0);
+                        }
                         mma_commit(bar(B_ACC_FULL + g));
                         ph = 1;
                         progress = true;
@@ -509,16 +525,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (mbar_test(bar(B_HP_READY + g), n & 1)) {
                         tc_fence_after();
                         // A = C (K-major), B = h_prev (MN-major)
-                        const uint64_t ca = sdesc(stage_c(st, 0), 16, 1024), db = sdesc(grp_w(g), kBox, 1024);
-                        for (int kk = 0; kk < 8; ++kk) {
+                        const uint64_t ca = sdesc(stage_c(st, 0), 16, 1024), db = sdesc(grp_hp(g), kBox, 1024);
+                        for (int kk = 0; kk < 8 * NS; ++kk) {
                             const uint64_t o = (uint64_t)((kk >> 2) * (kBox >> 4) + 2 * (kk & 3));
                             mma_ss(tmem + tm_Acc(g), ca + o, db + 128 * kk, id_yx, kk > 0);
                         }
                         mma_commit(bar(B_YO_FULL + g));
-                        if (j + 2 >= k) mma_commit(bar(B_CB_EMPTY + st));   // the group's last head of the item
+                        if (j + NG >= k) mma_commit(bar(B_CB_EMPTY + st));  // the group's last head of the item
                         ph = 0;
                         ++n;
-                        f += 2;
+                        f += NG;
                         it = f / k;
                         j = f - it * k;
                         progress = true;
@@ -528,9 +544,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int sidx = pubS[2 * g], blk = pubS[2 * g + 1];
                     if (sidx < 0) break;            // the group has finished every head
                     fence_acq_rel_gpu();
-                    unsigned *fl = p.flags + ((int64_t)sidx * 2 + (blk & 1)) * 4;
+                    unsigned *fl = p.flags + ((int64_t)sidx * 2 + (blk & 1)) * 4 * NS;
 #pragma unroll
-                    for (int qq = 0; qq < 4; ++qq) red_relaxed_add(fl + qq, 32u);
+                    for (int qq = 0; qq < 4 * NS; ++qq) red_relaxed_add(fl + qq, 32u);
                     mbar_arrive(bar(B_PUB_DONE + g));
                     ++m;
                     progress = true;
@@ -546,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-    } else {
+    } else if (warp >= 2 && warp < 2 + 4 * NG) {
         // ------------------------------------------------------------ math groups
         const int g = (warp - 2) >> 2;
         const int q = warp & 3;                 // TMEM lane quarter
@@ -555,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool leader = (warp == 2 + 4 * g) && lane == 0;
         float *cum = cumS + 128 * g;
         float *vq = vS + 512 * g;
-        float *adw = reinterpret_cast<float *>(smem + kOffAD) + 8 * (warp - 2);
+        float *adw = reinterpret_cast<float *>(smem + kOffAD) + 2 * kMaxK * (warp - 2);
         unsigned char *xbuf = smem + kOffGroup + g * kGroupBytes;
         unsigned char *wbuf = xbuf + kBox;
         {
@@ -571,23 +587,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         int it = 0, flat = 0, hcnt = 0, npub = 0;
         bool ok = true;
         for (;; ++it) {
-            const int st = it & 1;
-            if (!(ok = wait_bar(ctl, bar(B_CB_FULL + st), (it >> 1) & 1))) break;
+            const int st = it % NST;
+            if (!(ok = wait_bar(ctl, bar(B_CB_FULL + st), (it / NST) & 1))) break;
             const int id = itemS[st];
             if (id < 0) break;
             int bi, blk, hgi;
             decode_item(p, id, bi, blk, hgi);
             const int t0 = blk * kBlk;
             const int L = min(kBlk, p.T - t0);
-            const int j0 = (g - flat) & 1;      // first head of this group in the item
+            const int j0 = (g - flat % NG + NG) % NG;   // first head of this group in the item
             // C and B of this stage: bf16 -> fp16 in place, row r of all four boxes.  The
             // group that owns the item's first head does it: that group has no Y_off
             // of the previous item outstanding, so C B^T of this item never waits on
             // the other group's state chain.
             if (j0 == 0) {
-                unsigned char *base = smem + kOffStage + st * kStageBytes;
+                unsigned char *base = smem + kOffStage + st * kStage;
 #pragma unroll
-                for (int bx = 0; bx < 4; ++bx) {
+                for (int bx = 0; bx < 4 * NS; ++bx) {
                     uint4 *row = reinterpret_cast<uint4 *>(base + bx * kBox + r * 128);
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
@@ -611,12 +627,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // a thread-loaded dt tile is read (by every warp of both groups) only after all four
             // warps of the converting group have written their rows
-            if (!p.dt_tma && !(ok = wait_bar(ctl, bar(B_CB_CONV + st), (it >> 1) & 1))) break;
+            if (!p.dt_tma && !(ok = wait_bar(ctl, bar(B_CB_CONV + st), (it / NST) & 1))) break;
             const float *tile = dtT + st * (kBlk * kMaxK);
-            const int my_count = (k - j0 + 1) / 2;
+            const int my_count = (k - j0 + NG - 1) / NG;
             // A (log2 units) and D of this group's heads in the item, one copy per warp
             if (lane < my_count) {
-                const int hh = hgi * k + j0 + 2 * lane;
+                const int hh = hgi * k + j0 + NG * lane;
                 adw[2 * lane] = p.A[hh] * kLog2e;
                 adw[2 * lane + 1] = p.D ? p.D[hh] : 0.f;
             }
@@ -627,7 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (leader) mbar_arrive(bar(B_CB_EMPTY + st));
             }
             for (int s = 0; s < my_count && ok; ++s) {
-                const int j = j0 + 2 * s;
+                const int j = j0 + NG * s;
                 const int h = hgi * k + j;
                 const float Ah = adw[2 * s];
                 const float Dh = adw[2 * s + 1];
@@ -759,21 +775,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float a = ex2(total);
                     const float2 a2 = make_float2(a, a);
                     const int64_t sidx = (int64_t)bi * p.H + h;
-                    const int nrow = r;
                     const bool first = (blk == 0);
                     const bool last = (blk == p.nblk - 1);
+                    unsigned char *hpbuf = smem + (grp_hp(g) - sbase);
+                    // one pass per 128 state rows (N = 256: rows r and r + 128 of this thread)
+#pragma unroll 1
+                    for (int hf = 0; hf < NS; ++hf) {
+                    const int nrow = r + 128 * hf;
                     // Ring slots are chunk-major -- float4 chunk e of state row n at
-                    // (e * 128 + n) -- so each warp-wide access is 512 contiguous bytes.
+                    // (e * N + n) -- so each warp-wide access is 512 contiguous bytes.
                     // init_state / final_state keep the caller's (N, P) row-major layout.
-                    // A slot's counter (one per 32 state rows) grows by 32 per publication,
-                    // one release add per row.
+                    // A slot's counter (one per 32 state rows) grows by 32 per publication.
                     const float4 *src = nullptr;
                     int src_stride = 1;                 // float4 step between chunks of a row
                     if (first) {
-                        if (p.init) src = reinterpret_cast<const float4 *>(p.init + (sidx * kN + nrow) * kP);
+                        if (p.init) src = reinterpret_cast<const float4 *>(p.init + (sidx * kNr + nrow) * kP);
                     } else {
                         const int ps = (blk - 1) & 1;
-                        const unsigned *fl = p.flags + (sidx * 2 + ps) * 4 + q;
+                        const unsigned *fl = p.flags + (sidx * 2 + ps) * 4 * NS + q + 4 * hf;
                         const unsigned want = 32u * (unsigned)((blk - 1) / 2 + 1);
                         bool got = false;
                         for (int64_t i = 0; i < p.chain_spin; ++i) {
@@ -783,8 +802,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                         }
                         if (got) {
-                            src = reinterpret_cast<const float4 *>(p.ring + (sidx * 2 + ps) * kN * kP) + nrow;
-                            src_stride = kN;
+                            src = reinterpret_cast<const float4 *>(p.ring + (sidx * 2 + ps) * kNr * kP) + nrow;
+                            src_stride = kNr;
                         } else {
                             set_status(p.status, SSD_ERR_TIMEOUT);
                         }
@@ -792,10 +811,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float4 *dst = nullptr;
                     int dst_stride = 1;
                     if (last) {
-                        if (p.final_state) dst = reinterpret_cast<float4 *>(p.final_state + (sidx * kN + nrow) * kP);
+                        if (p.final_state) dst = reinterpret_cast<float4 *>(p.final_state + (sidx * kNr + nrow) * kP);
                     } else {
-                        dst = reinterpret_cast<float4 *>(p.ring + (sidx * 2 + (blk & 1)) * kN * kP) + nrow;
-                        dst_stride = kN;
+                        dst = reinterpret_cast<float4 *>(p.ring + (sidx * 2 + (blk & 1)) * kNr * kP) + nrow;
+                        dst_stride = kNr;
                     }
                     float4 hp[16];
                     if (src) {
@@ -810,7 +829,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
                         float sv[32];
-                        tmem_ld32(tmem + lane_off + tm_Acc(g) + 32 * half, sv);
+                        tmem_ld32(tmem + lane_off + tm_Acc(g) + 64 * hf + 32 * half, sv);
                         tmem_ld_wait();
 #pragma unroll
                         for (int e8 = 0; e8 < 8; ++e8) {
@@ -828,8 +847,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
 #pragma unroll
                     for (int cc = 0; cc < 8; ++cc)
-                        *reinterpret_cast<uint4 *>(wbuf + swz(nrow, cc)) =
+                        *reinterpret_cast<uint4 *>(hpbuf + swz(nrow, cc)) =
                             make_uint4(hk[4 * cc], hk[4 * cc + 1], hk[4 * cc + 2], hk[4 * cc + 3]);
+                    }
                     fence_async_smem();
                     tc_fence_before();
                     __syncwarp();
@@ -965,7 +985,10 @@ int heads_per_item(const Problem &p) {
     return k;
 }
 
-size_t flags_bytes(const Problem &p) { return align_up(sizeof(unsigned) * (size_t)(p.b * p.H * 2 * 4), 256); }
+// one counter per (batch, head, ring slot, 32 state rows)
+size_t flags_bytes(const Problem &p) {
+    return align_up(sizeof(unsigned) * (size_t)(p.b * p.H * 2 * (p.N / 32)), 256);
+}
 
 // Per-device launch setup, done once per device: SM count and the kernel's
 // dynamic shared memory limit.  Returns the SM count (0 on failure).
@@ -980,8 +1003,10 @@ int device_setup() {
     if (sms[dev] == 0) {
         int n = 0;
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-        if (cudaFuncSetAttribute(ssd_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
-            cudaSuccess)
+        if (cudaFuncSetAttribute(ssd_fused_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+                cudaSuccess ||
+            cudaFuncSetAttribute(ssd_fused_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+                cudaSuccess)
             return 0;
         sms[dev] = n;
     }
@@ -992,7 +1017,7 @@ int device_setup() {
 
 bool fused_supports(const Problem &p) {
     if (p.a_mode != SSD_A_SCALAR || p.io_dtype != SSD_DTYPE_BF16) return false;
-    if (p.P != kP || p.N != kN) return false;
+    if (p.P != kP || (p.N != 128 && p.N != 256)) return false;
     if (p.Q != 128 && p.Q != 256) return false;
     if (p.T > (int64_t)INT32_MAX / 2 || p.b * p.H * 2 > (int64_t)INT32_MAX) return false;
     const int64_t items = ((p.T + kBlk - 1) / kBlk) * p.b * (p.H / heads_per_item(p));
@@ -1000,7 +1025,7 @@ bool fused_supports(const Problem &p) {
 }
 
 size_t fused_workspace_bytes(const Problem &p) {
-    return kStatusBytes + flags_bytes(p) + sizeof(float) * (size_t)(p.b * p.H * 2 * kN * kP);
+    return kStatusBytes + flags_bytes(p) + sizeof(float) * (size_t)(p.b * p.H * 2 * p.N * kP);
 }
 
 cudaError_t fused_launch(const Problem &p, void *ws, size_t ws_bytes, cudaStream_t s) {
@@ -1045,7 +1070,10 @@ cudaError_t fused_launch(const Problem &p, void *ws, size_t ws_bytes, cudaStream
     if (sms <= 0) return cudaErrorInvalidDevice;
     const int grid = fp.total_items < sms ? fp.total_items : sms;
     record_dominant_start(s);
-    ssd_fused_kernel<<<grid, kThreads, kSmemBytes, s>>>(mx, mB, mC, my, mdt, fp);
+    if (p.N == 128)
+        ssd_fused_kernel<1><<<grid, kThreads, kSmemBytes, s>>>(mx, mB, mC, my, mdt, fp);
+    else
+        ssd_fused_kernel<2><<<grid, kThreads, kSmemBytes, s>>>(mx, mB, mC, my, mdt, fp);
     record_dominant_stop(s);
     note_launches(1);
     return cudaGetLastError();

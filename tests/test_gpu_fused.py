@@ -69,7 +69,12 @@ def test_withheld_state_reports_timeout_and_context_survives(cuda_device):
     Workload("t", b=2, T=8192, H=16, P=64, N=128, G=2, Q=256, D="normal", init_std=0.1, seed=74),
     # odd heads per item (k = 5): consecutive items start on alternating math groups
     Workload("t", b=3, T=4000, H=10, P=64, N=128, G=2, Q=128, D="none", seed=75),
-], ids=["k4_g2", "one_head_per_group", "k5_ragged130", "many_items_per_cta", "odd_k_many_items"])
+    # N = 256 (one math group, one C/B stage, two state accumulators): 4 heads per group
+    Workload("t", b=1, T=1500, H=8, P=64, N=256, G=2, Q=128, D="normal", init_std=0.1, seed=76),
+    # N = 256 with several items per CTA, k = 3 (dt by thread loads), Q = 256
+    Workload("t", b=2, T=9000, H=6, P=64, N=256, G=2, Q=256, D="none", init_std=0.1, seed=77),
+], ids=["k4_g2", "one_head_per_group", "k5_ragged130", "many_items_per_cta", "odd_k_many_items",
+        "n256_k4", "n256_many_items_k3"])
 def test_fused_matches_generic_and_oracle(w, cuda_device):
     assert _fused_ok(w)
     inp = make_inputs(w)
