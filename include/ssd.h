@@ -95,10 +95,10 @@ typedef struct ssd_dims {
 
 /* Paths.  SSD_PATH_TCGEN05 (one fused persistent kernel: TMA loads, tcgen05
  * tensor-core products with TMEM accumulators, block-to-block state hand-off
- * through an L2-resident ring) takes scalar A, bf16 io, P == 64, N == 128 and
- * Q in {128, 256}; it evaluates every chunk as 128-token blocks (for Q = 256,
- * two blocks per chunk -- the chunked algorithm applied inside the chunk,
- * equal up to rounding).  SSD_PATH_GENERIC (fp32 CUDA-core kernels) takes
+ * through an L2-resident ring) takes scalar A, bf16 io, P == 64, N in
+ * {128, 256} and Q in {128, 256}; it evaluates every chunk as 128-token blocks
+ * (for Q = 256, two blocks per chunk -- the chunked algorithm applied inside
+ * the chunk, equal up to rounding).  SSD_PATH_GENERIC (fp32 CUDA-core kernels) takes
  * every dims the ABI accepts.  SSD_PATH_AUTO picks TCGEN05 where it applies.
  *
  * Bytes of device workspace ssd_fwd needs for `dims` (written to *bytes).
