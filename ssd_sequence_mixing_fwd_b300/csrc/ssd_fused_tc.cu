@@ -72,8 +72,8 @@ constexpr int kOffDt = kOffV + 2 * 4 * 128 * 4;             // float [2 stages][
 constexpr int kOffItem = kOffDt + 2 * 128 * kMaxK * 4;      // int [2]
 constexpr int kOffMisc = kOffItem + 2 * 4;                  // tmem base, abort
 constexpr int kOffPub = kOffMisc + 16;                      // int [2][2]: (stream, block) mailbox
-constexpr int kOffAD = kOffPub + 16;                        // float [8 warps][2 kMaxK]: A, D of the item's heads
-constexpr int kOffBar = ((kOffAD + 8 * 2 * kMaxK * 4 + 7) / 8) * 8;  // mbarriers
+constexpr int kOffAD = kOffPub + 16;                        // float [2 stages][kMaxK][2]: A (log2 units), D
+constexpr int kOffBar = ((kOffAD + 2 * 2 * kMaxK * 4 + 7) / 8) * 8;  // mbarriers
 constexpr int kNumBars = 32;
 constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 1024;   // + alignment slack
 
@@ -424,6 +424,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 decode_item(p, id, bi, blk, hgi);
                 const int t0 = blk * kBlk;
                 const int grp = (hgi * k) / (p.H / p.G);
+                {
+                    float *ad = reinterpret_cast<float *>(smem + kOffAD) + st * (2 * kMaxK);
+                    float av[kMaxK], dv[kMaxK];
+#pragma unroll
+                    for (int jj = 0; jj < kMaxK; ++jj) {
+                        av[jj] = jj < k ? p.A[hgi * k + jj] : 0.f;
+                        dv[jj] = (jj < k && p.D) ? p.D[hgi * k + jj] : 0.f;
+                    }
+#pragma unroll
+                    for (int jj = 0; jj < kMaxK; ++jj) {
+                        ad[2 * jj] = av[jj] * kLog2e;
+                        ad[2 * jj + 1] = dv[jj];
+                    }
+                }
                 mbar_expect_tx(bar(B_CB_FULL + st), kStage + (p.dt_tma ? kBlk * k * 4 : 0));
                 last_cb_use[st] = it;
                 if (p.dt_tma) tma_load_3d(sbase + kOffDt + st * (kBlk * kMaxK * 4), &tm_dt, bar(B_CB_FULL + st),
@@ -571,7 +585,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool leader = (warp == 2 + 4 * g) && lane == 0;
         float *cum = cumS + 128 * g;
         float *vq = vS + 512 * g;
-        float *adw = reinterpret_cast<float *>(smem + kOffAD) + 2 * kMaxK * (warp - 2);
         unsigned char *xbuf = smem + kOffGroup + g * kGroupBytes;
         unsigned char *wbuf = xbuf + kBox;
         {
@@ -602,17 +615,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the other group's state chain.
             if (j0 == 0) {
                 unsigned char *base = smem + kOffStage + st * kStage;
-#pragma unroll
+                // chunk c ^ (r & 7): eight consecutive rows touch eight different 16-byte
+                // bank groups (walking chunk c of every row would put a quarter warp on
+                // the same four banks)
+                const uint32_t rx = (uint32_t)(r & 7) * 16u;
+#pragma unroll 1
                 for (int bx = 0; bx < 4 * NS; ++bx) {
-                    uint4 *row = reinterpret_cast<uint4 *>(base + bx * kBox + r * 128);
+                    unsigned char *row = base + bx * kBox + r * 128;
+                    uint4 u[8];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) u[c] = *reinterpret_cast<const uint4 *>(row + ((16u * c) ^ rx));
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
-                        uint4 u = row[c];
-                        u.x = bf2_to_h2(u.x);
-                        u.y = bf2_to_h2(u.y);
-                        u.z = bf2_to_h2(u.z);
-                        u.w = bf2_to_h2(u.w);
-                        row[c] = u;
+                        u[c].x = bf2_to_h2(u[c].x);
+                        u[c].y = bf2_to_h2(u[c].y);
+                        u[c].z = bf2_to_h2(u[c].z);
+                        u[c].w = bf2_to_h2(u[c].w);
+                        *reinterpret_cast<uint4 *>(row + ((16u * c) ^ rx)) = u[c];
                     }
                 }
                 if (!p.dt_tma) {
@@ -630,13 +649,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!p.dt_tma && !(ok = wait_bar(ctl, bar(B_CB_CONV + st), (it / NST) & 1))) break;
             const float *tile = dtT + st * (kBlk * kMaxK);
             const int my_count = (k - j0 + NG - 1) / NG;
-            // A (log2 units) and D of this group's heads in the item, one copy per warp
-            if (lane < my_count) {
-                const int hh = hgi * k + j0 + NG * lane;
-                adw[2 * lane] = p.A[hh] * kLog2e;
-                adw[2 * lane + 1] = p.D ? p.D[hh] : 0.f;
-            }
-            __syncwarp();
+            // A (log2 units) and D of the item's heads: written by the producer with the stage
+            const float *adS = reinterpret_cast<const float *>(smem + kOffAD) + st * (2 * kMaxK);
             if (my_count == 0) {
                 // no head of this item here: nothing of this group reads C B^T or the stage
                 if (lane == 0) mbar_arrive(bar(B_CBTMEM_EMPTY));
@@ -645,8 +659,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < my_count && ok; ++s) {
                 const int j = j0 + NG * s;
                 const int h = hgi * k + j;
-                const float Ah = adw[2 * s];
-                const float Dh = adw[2 * s + 1];
+                const float Ah = adS[2 * j];
+                const float Dh = adS[2 * j + 1];
                 // (1) cum (log2 units) over the block, per warp and without group barriers:
                 //     each warp scans the quarters up to its own (lane = row within a quarter),
                 //     keeps cum of its own rows (diagonal block) and the rank-1 factors
