@@ -307,8 +307,10 @@ __device__ __forceinline__ void set_status(int *status, int code) { atomicCAS(st
 
 // Waits for `parity` of `bar`; false (and the CTA marked aborting) when the
 // iteration limit runs out or another thread of the CTA gave up already.
-__device__ __forceinline__ bool wait_bar(const Ctl &c, uint32_t bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
+// The retry loop is a called function, not inlined at each of the many wait
+// sites: the kernel's hot loop has to fit the instruction cache (inlined, the
+// copies made the N = 128 kernel about 18 KB larger and measurably slower).
+__device__ __noinline__ bool wait_bar_slow(const Ctl &c, uint32_t bar, uint32_t parity) {
     for (uint32_t i = 0; i < kBarSpin; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 255u) == 255u && *c.abort_flag) return false;
@@ -316,6 +318,10 @@ __device__ __forceinline__ bool wait_bar(const Ctl &c, uint32_t bar, uint32_t pa
     set_status(c.status, SSD_ERR_TIMEOUT);
     *c.abort_flag = 1;
     return false;
+}
+__device__ __forceinline__ bool wait_bar(const Ctl &c, uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_bar_slow(c, bar, parity);
 }
 
 // Bounded wait that ignores the abort flag (used while winding down).
@@ -750,10 +756,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 {
                     const float u = ex2(ci - Rq);
                     const float2 u2 = make_float2(u, u);
-                    // column blocks J > q stay zero: written once per CTA before the loop
-#pragma unroll
-                    for (int J = 0; J < 4; ++J) {
-                        if (J > q) continue;
+                    // column blocks J > q stay zero: written once per CTA before the loop.
+                    // (a rolled loop: unrolled over J it made the kernel ~11 KB larger, and
+                    // code size, through the instruction cache, costs more than the loop)
+#pragma unroll 1
+                    for (int J = 0; J <= q; ++J) {
                         uint32_t pk[16];
                         float c[32];
                         tmem_ld32(tmem + lane_off + kTmCB + 32 * J, c);
