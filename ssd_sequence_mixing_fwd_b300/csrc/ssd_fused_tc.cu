@@ -99,9 +99,9 @@ constexpr int B_Y_READY = 30;       // [2] all rows of y are in the W buffer (4 
 
 // TMEM columns (512 allocated)
 constexpr uint32_t kTmCB = 0;                       // 128 cols: C B^T (fp32)
-__host__ __device__ constexpr uint32_t tm_S(int g) { return 128 + 192 * g; }     // 64 cols fp16x2
+__host__ __device__ constexpr uint32_t tm_S(int g) { return 128 + 192 * g; }     // 64 cols: S (fp16 pairs); N = 128: then Y_off
 __host__ __device__ constexpr uint32_t tm_Yd(int g) { return 192 + 192 * g; }    // 64 cols
-__host__ __device__ constexpr uint32_t tm_Acc(int g) { return 256 + 192 * g; }   // 64 cols: s, then Y_off
+__host__ __device__ constexpr uint32_t tm_Acc(int g) { return 256 + 192 * g; }   // 64 cols: s (N = 256: 128 cols, then Y_off)
 
 // Wait limits.  One try_wait suspends for at most about kSuspendNs, so an
 // mbarrier wait gives up after roughly kBarSpin * kSuspendNs (about 2 s); a
@@ -503,7 +503,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         //    visible and the 32-row counters of the ring slot grow by 32;
         //  * products of the group's current head, each as soon as its inputs are ready:
         //    s = B^T (w o X), then Y_diag (+)= S X (its completion frees the X buffer),
-        //    then Y_off = C h_prev (after the item's last one, the stage's C/B are released).
+        //    then Y_off = C h_prev (after the item's last one, the stage's C/B are released;
+        //    N = 128 writes it into the S columns once S X has completed).
         const int g = warp - 10;
         if (lane == 0) {
             const uint32_t id_st = idesc_f16(128, kP, 1, 1);
@@ -542,13 +543,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         progress = true;
                     }
                 } else {
-                    if (mbar_test(bar(B_HP_READY + g), n & 1)) {
+                    // (N = 128: C h_prev writes the S columns, so S X must have completed)
+                    if (mbar_test(bar(B_HP_READY + g), n & 1) && (NS == 2 || mbar_test(bar(B_X_EMPTY + g), n & 1))) {
                         tc_fence_after();
                         // A = C (K-major), B = h_prev (MN-major)
                         const uint64_t ca = sdesc(stage_c(st, 0), 16, 1024), db = sdesc(grp_hp(g), kBox, 1024);
                         for (int kk = 0; kk < 8 * NS; ++kk) {
                             const uint64_t o = (uint64_t)((kk >> 2) * (kBox >> 4) + 2 * (kk & 3));
-                            mma_ss(tmem + tm_Acc(g), ca + o, db + 128 * kk, id_yx, kk > 0);
+                            mma_ss(tmem + (NS == 1 ? tm_S(g) : tm_Acc(g)), ca + o, db + 128 * kk, id_yx, kk > 0);
                         }
                         mma_commit(bar(B_YO_FULL + g));
                         if (j + NG >= k) mma_commit(bar(B_CB_EMPTY + st));  // the group's last head of the item
@@ -789,7 +791,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (s == my_count - 1) mbar_arrive(bar(B_CBTMEM_EMPTY));
                     }
                 }
-                // (4) state step: h = 2^total h_prev + s; publish; h_prev (fp16) -> W buffer
+                // (4) state step: h_prev (fp16) -> W buffer for C h_prev; h = 2^total h_prev + s; publish
                 if (!(ok = wait_bar(ctl, bar(B_ACC_FULL + g), hcnt & 1))) break;
                 tc_fence_after();
                 {
@@ -846,6 +848,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int e = 0; e < 16; ++e) hp[e] = make_float4(0.f, 0.f, 0.f, 0.f);
                     }
                     uint32_t hk[32];                    // h_prev as fp16 pairs, for C h_prev
+                    if constexpr (NS == 1) {
+                        // N = 128: C h_prev goes to the S columns (free once S X has completed:
+                        // the issuer also waits for that), so it needs h_prev only and is
+                        // signalled before s is read and before the global stores, whose
+                        // completion the release of this arrive would otherwise wait for
+#pragma unroll
+                        for (int cc = 0; cc < 8; ++cc) {
+                            const float4 u0 = hp[2 * cc], u1 = hp[2 * cc + 1];
+                            *reinterpret_cast<uint4 *>(hpbuf + swz(nrow, cc)) =
+                                make_uint4(pack_h2(u0.x, u0.y), pack_h2(u0.z, u0.w), pack_h2(u1.x, u1.y), pack_h2(u1.z, u1.w));
+                        }
+                        fence_async_smem();
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar(B_HP_READY + g));
+                    }
                     // s is read from TMEM while the global loads are in flight
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
@@ -862,19 +880,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                        make_float2(sv[4 * e8 + 2], sv[4 * e8 + 3]));
                                 __stcg(dst + e * dst_stride, make_float4(lo.x, lo.y, hi.x, hi.y));
                             }
-                            hk[2 * e] = pack_h2(t4.x, t4.y);
-                            hk[2 * e + 1] = pack_h2(t4.z, t4.w);
+                            if constexpr (NS == 2) {
+                                hk[2 * e] = pack_h2(t4.x, t4.y);
+                                hk[2 * e + 1] = pack_h2(t4.z, t4.w);
+                            }
                         }
                     }
+                    if constexpr (NS == 2) {
 #pragma unroll
-                    for (int cc = 0; cc < 8; ++cc)
-                        *reinterpret_cast<uint4 *>(hpbuf + swz(nrow, cc)) =
-                            make_uint4(hk[4 * cc], hk[4 * cc + 1], hk[4 * cc + 2], hk[4 * cc + 3]);
+                        for (int cc = 0; cc < 8; ++cc)
+                            *reinterpret_cast<uint4 *>(hpbuf + swz(nrow, cc)) =
+                                make_uint4(hk[4 * cc], hk[4 * cc + 1], hk[4 * cc + 2], hk[4 * cc + 3]);
                     }
-                    fence_async_smem();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(B_HP_READY + g));
+                    }
+                    if constexpr (NS == 2) {
+                        fence_async_smem();
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar(B_HP_READY + g));
+                    }
                     if (!last && (int64_t)blk != p.withhold) {
                         // Hand the publication to this group's issuer warp, which makes the
                         // stores visible at GPU scope (fence) and bumps the counters, so these
@@ -903,7 +927,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int half = 0; half < 2; ++half) {
                         float yd[32], yo[32];
                         tmem_ld32(tmem + lane_off + tm_Yd(g) + 32 * half, yd);
-                        tmem_ld32(tmem + lane_off + tm_Acc(g) + 32 * half, yo);
+                        tmem_ld32(tmem + lane_off + (NS == 1 ? tm_S(g) : tm_Acc(g)) + 32 * half, yo);
                         tmem_ld_wait();
 #pragma unroll
                         for (int cc = 0; cc < 4; ++cc) {
@@ -918,6 +942,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                             *reinterpret_cast<uint4 *>(wbuf + swz(r, 4 * half + cc)) =
                                 make_uint4(ow[0], ow[1], ow[2], ow[3]);
                         }
+                    }
+                    if constexpr (NS == 1) {
+                        // C h_prev overwrote the zero blocks right of this quarter's diagonal:
+                        // restore them for the next head's S
+                        uint32_t z[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) z[e] = 0u;
+#pragma unroll
+                        for (int J = 1; J < 4; ++J)
+                            if (J > q) tmem_st16(tmem + lane_off + tm_S(g) + 16 * J, z);
                     }
                     tc_fence_before();
                     fence_async_smem();
