@@ -66,8 +66,8 @@ constexpr int kBox = kBlk * 64 * 2;                 // one 128 x 64 fp16 box: 16
 constexpr int kOffStage = 0;                        // 2 stages
 constexpr int kOffGroup = 8 * kBox;                 // per math group: X, W (N = 256: group 1's space holds h_prev)
 constexpr int kGroupBytes = 2 * kBox;
-constexpr int kOffCum = kOffGroup + 2 * kGroupBytes;        // float [2][128]
-constexpr int kOffV = kOffCum + 2 * 128 * 4;                // float [2][4][128]
+constexpr int kOffCum = kOffGroup + 2 * kGroupBytes;        // float [2 stages][kMaxK][128]: cum of each head
+constexpr int kOffV = kOffCum + 2 * kMaxK * 128 * 4;        // float [2][4][128]
 constexpr int kOffDt = kOffV + 2 * 4 * 128 * 4;             // float [2 stages][128][kMaxK]: dt tile
 constexpr int kOffItem = kOffDt + 2 * 128 * kMaxK * 4;      // int [2]
 constexpr int kOffMisc = kOffItem + 2 * 4;                  // tmem base, abort
@@ -90,8 +90,7 @@ constexpr int B_S_READY = 14;       // [2] S written to TMEM (4 warps)
 constexpr int B_ACC_FULL = 16;      // [2] Y_diag and s are in TMEM
 constexpr int B_HP_READY = 18;      // [2] h_prev (fp16) written, s read (4 warps)
 constexpr int B_YO_FULL = 20;       // [2] Y_off is in TMEM
-// 22-23 unused: a head's XW_READY arrival follows each warp's epilogue of the
-// group's previous head, so it also says that head's TMEM columns are free
+constexpr int B_CUM_READY = 22;     // [2] cum of every head of the stage's item is in shared memory
 constexpr int B_PUB_FULL = 24;      // [2] a group stored a state: publish it (4 warps)
 constexpr int B_PUB_DONE = 26;      // [2] the publisher has taken the mailbox
 constexpr int B_W_FREE = 28;        // [2] the previous y store has read the W buffer (leader)
@@ -356,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int NST = (NS == 1) ? 2 : 1;
     constexpr int kStage = 4 * NS * kBox;
 
-    float *cumS = reinterpret_cast<float *>(smem + kOffCum);     // [2][128]
+    float *cumT = reinterpret_cast<float *>(smem + kOffCum);     // [2 stages][kMaxK][128]
     float *vS = reinterpret_cast<float *>(smem + kOffV);         // [2][4][128]
     float *dtT = reinterpret_cast<float *>(smem + kOffDt);       // [2][128][k]
     int *itemS = reinterpret_cast<int *>(smem + kOffItem);       // [2]
@@ -387,6 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(B_ACC_FULL + s), 1);
             mbar_init(bar(B_HP_READY + s), 4);
             mbar_init(bar(B_YO_FULL + s), 1);
+            mbar_init(bar(B_CUM_READY + s), 1);
         }
         mbar_init(bar(B_CBMMA_FULL), 1);
         mbar_init(bar(B_CBTMEM_EMPTY), 4 * NG);
@@ -472,26 +472,63 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------------ C B^T issuer
-        // Owns TMEM; issues each item's C B^T once its C and B are fp16 and every
-        // mask of the previous item has read the previous C B^T.
-        if (lane == 0) {
+        // ------------------------------------------------------------ prefix sums + C B^T issuer
+        // Per item, the whole warp computes cum_t = sum_{u <= t} dt_u A log2(e) of each of
+        // the item's heads into shared memory (four interleaved 32-row scans, rows
+        // lane + 32 m), so the math groups start a head without a scan.  Lane 0 owns TMEM
+        // and issues the item's C B^T once its C and B are fp16 and every mask of the
+        // previous item has read the previous C B^T.
+        {
             const uint32_t id_cb = idesc_f16(128, 128, 0, 0);
             for (int it = 0;; ++it) {
                 const int st = it % NST;
                 const uint32_t par = (it / NST) & 1;
-                if (!wait_bar(ctl, bar(B_CB_FULL + st), par)) break;
+                // every lane waits (no lane idles at a shuffle while another waits); a vote
+                // keeps the lanes together when a wait gives up
+                if (!__all_sync(0xffffffffu, wait_bar(ctl, bar(B_CB_FULL + st), par))) break;
                 if (itemS[st] < 0) break;
-                if (!wait_bar(ctl, bar(B_CB_CONV + st), par)) break;
-                if (it >= 1 && !wait_bar(ctl, bar(B_CBTMEM_EMPTY), (it - 1) & 1)) break;
-                tc_fence_after();
-                // K steps of 16: +32 bytes inside a swizzle atom, next atom = next box
-                const uint64_t ca = sdesc(stage_c(st, 0), 16, 1024), cb = sdesc(stage_b(st, 0), 16, 1024);
-                for (int kk = 0; kk < 8 * NS; ++kk) {
-                    const uint64_t o = (uint64_t)((kk >> 2) * (kBox >> 4) + 2 * (kk & 3));
-                    mma_ss(tmem + kTmCB, ca + o, cb + o, id_cb, kk > 0);
+                if (!p.dt_tma && !__all_sync(0xffffffffu, wait_bar(ctl, bar(B_CB_CONV + st), par))) break;
+                {
+                    const float *tile = dtT + st * (kBlk * kMaxK);
+                    const float *adS = reinterpret_cast<const float *>(smem + kOffAD) + st * (2 * kMaxK);
+                    float *ct = cumT + st * (kMaxK * 128);
+                    for (int jj = 0; jj < k; ++jj) {
+                        // rows lane + 32 m: four interleaved 32-row scans, then the quarter offsets
+                        const float Aj = adS[2 * jj];
+                        float v[4];
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) v[m] = tile[(32 * m + lane) * k + jj] * Aj;
+#pragma unroll
+                        for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+                            for (int m = 0; m < 4; ++m) {
+                                const float u2 = __shfl_up_sync(0xffffffffu, v[m], o);
+                                if (lane >= o) v[m] += u2;
+                            }
+                        }
+                        float run = 0.f;
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) {
+                            ct[jj * 128 + 32 * m + lane] = run + v[m];
+                            run += __shfl_sync(0xffffffffu, v[m], 31);
+                        }
+                    }
                 }
-                mma_commit(bar(B_CBMMA_FULL));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_CUM_READY + st));
+                if (!__all_sync(0xffffffffu, wait_bar(ctl, bar(B_CB_CONV + st), par))) break;
+                if (it >= 1 && !__all_sync(0xffffffffu, wait_bar(ctl, bar(B_CBTMEM_EMPTY), (it - 1) & 1))) break;
+                if (lane == 0) {
+                    tc_fence_after();
+                    // K steps of 16: +32 bytes inside a swizzle atom, next atom = next box
+                    const uint64_t ca = sdesc(stage_c(st, 0), 16, 1024), cb = sdesc(stage_b(st, 0), 16, 1024);
+                    for (int kk = 0; kk < 8 * NS; ++kk) {
+                        const uint64_t o = (uint64_t)((kk >> 2) * (kBox >> 4) + 2 * (kk & 3));
+                        mma_ss(tmem + kTmCB, ca + o, cb + o, id_cb, kk > 0);
+                    }
+                    mma_commit(bar(B_CBMMA_FULL));
+                }
+                __syncwarp();
             }
         }
     } else if (warp >= 10 && warp < 10 + NG) {
@@ -591,7 +628,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = 32 * q + lane;            // row of this thread (token or state row)
         const uint32_t lane_off = (uint32_t)(32 * q) << 16;
         const bool leader = (warp == 2 + 4 * g) && lane == 0;
-        float *cum = cumS + 128 * g;
         float *vq = vS + 512 * g;
         unsigned char *xbuf = smem + kOffGroup + g * kGroupBytes;
         unsigned char *wbuf = xbuf + kBox;
@@ -652,13 +688,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(B_CB_CONV + st));
             }
-            // a thread-loaded dt tile is read (by every warp of both groups) only after all four
-            // warps of the converting group have written their rows
-            if (!p.dt_tma && !(ok = wait_bar(ctl, bar(B_CB_CONV + st), (it / NST) & 1))) break;
-            const float *tile = dtT + st * (kBlk * kMaxK);
             const int my_count = (k - j0 + NG - 1) / NG;
             // A (log2 units) and D of the item's heads: written by the producer with the stage
             const float *adS = reinterpret_cast<const float *>(smem + kOffAD) + st * (2 * kMaxK);
+            // the prefix sums of the item's heads (warp 1; it reads a thread-loaded dt tile only
+            // after the converting group has written it)
+            if (my_count > 0 && !(ok = wait_bar(ctl, bar(B_CUM_READY + st), (it / NST) & 1))) break;
             if (my_count == 0) {
                 // no head of this item here: nothing of this group reads C B^T or the stage
                 if (lane == 0) mbar_arrive(bar(B_CBTMEM_EMPTY));
@@ -667,44 +702,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < my_count && ok; ++s) {
                 const int j = j0 + NG * s;
                 const int h = hgi * k + j;
-                const float Ah = adS[2 * j];
                 const float Dh = adS[2 * j + 1];
-                // (1) cum (log2 units) over the block, per warp and without group barriers:
-                //     each warp scans the quarters up to its own (lane = row within a quarter),
-                //     keeps cum of its own rows (diagonal block) and the rank-1 factors
-                //     v_j = 2^(R - cum_j), R = cum at row 32q - 1, for the rows below.
-                // the four quarter scans are independent until their offsets: interleaved
-                float vv4[4];
-#pragma unroll
-                for (int m = 0; m < 4; ++m) vv4[m] = tile[(32 * m + lane) * k + j] * Ah;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        const float u2 = __shfl_up_sync(0xffffffffu, vv4[m], o);
-                        if (lane >= o) vv4[m] += u2;
-                    }
-                }
-                float qs[4];
-#pragma unroll
-                for (int m = 0; m < 4; ++m) qs[m] = __shfl_sync(0xffffffffu, vv4[m], 31);
-                float ci = 0.f, run = 0.f, Rq = 0.f;
-                float cm[3];
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const float c_m = run + vv4[m];
-                    if (m < 3) cm[m] = c_m;
-                    if (m == q) {
-                        ci = c_m;
-                        Rq = run;
-                    }
-                    run += qs[m];
-                }
-                const float total = run;
-                cum[r] = ci;                            // own rows only (diagonal block)
+                // (1) cum (log2 units) of this head, computed per item by warp 1: own row ci,
+                //     the block total, R = cum at row 32q - 1, and the rank-1 factors
+                //     v_j = 2^(R - cum_j) of the rows of earlier quarters
+                const float *cum = cumT + st * (kMaxK * 128) + j * 128;
+                const float ci = cum[r];
+                const float total = cum[127];
+                const float Rq = q ? cum[32 * q - 1] : 0.f;
 #pragma unroll
                 for (int m = 0; m < 3; ++m)
-                    if (m < q) vq[128 * q + 32 * m + lane] = ex2(Rq - cm[m]);
+                    if (m < q) vq[128 * q + 32 * m + lane] = ex2(Rq - cum[32 * m + lane]);
                 __syncwarp();
                 // (2) X -> fp16 in place (for S X); w o X -> W; Y_diag <- D x (exact fp32, the
                 //     S X products accumulate onto it)
