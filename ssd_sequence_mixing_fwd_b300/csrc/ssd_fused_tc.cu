@@ -600,12 +600,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (mbar_test(bar(B_PUB_FULL + g), m & 1)) {
-                    const int sidx = pubS[2 * g], blk = pubS[2 * g + 1];
+                    const int sidx = pubS[2 * g], bh = pubS[2 * g + 1];
                     if (sidx < 0) break;            // the group has finished every head
                     fence_acq_rel_gpu();
-                    unsigned *fl = p.flags + ((int64_t)sidx * 2 + (blk & 1)) * 4 * NS;
+                    // bh = 2 block + half: the four 32-row counters of one 128-row half
+                    unsigned *fl = p.flags + ((int64_t)sidx * 2 + ((bh >> 1) & 1)) * 4 * NS + 4 * (bh & 1);
 #pragma unroll
-                    for (int qq = 0; qq < 4 * NS; ++qq) red_relaxed_add(fl + qq, 32u);
+                    for (int qq = 0; qq < 4; ++qq) red_relaxed_add(fl + qq, 32u);
                     mbar_arrive(bar(B_PUB_DONE + g));
                     ++m;
                     progress = true;
@@ -899,6 +900,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int cc = 0; cc < 8; ++cc)
                             *reinterpret_cast<uint4 *>(hpbuf + swz(nrow, cc)) =
                                 make_uint4(hk[4 * cc], hk[4 * cc + 1], hk[4 * cc + 2], hk[4 * cc + 3]);
+                        // N = 256: rows 0-127 are published as soon as they are stored, so the
+                        // next block's first half need not wait for this block's second half
+                        if (hf == 0 && !last && (int64_t)blk != p.withhold) {
+                            if (leader) {
+                                if (npub >= 1) wait_bar(ctl, bar(B_PUB_DONE + g), (npub - 1) & 1);
+                                pubS[2 * g] = (int)sidx;
+                                pubS[2 * g + 1] = 2 * blk;
+                            }
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(bar(B_PUB_FULL + g));
+                            ++npub;
+                        }
                     }
                     }
                     if constexpr (NS == 2) {
@@ -917,7 +930,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             // other waits then end quickly)
                             if (npub >= 1) wait_bar(ctl, bar(B_PUB_DONE + g), (npub - 1) & 1);
                             pubS[2 * g] = (int)sidx;
-                            pubS[2 * g + 1] = blk;
+                            pubS[2 * g + 1] = 2 * blk + (NS - 1);   // N = 256: the second half
                         }
                         __syncwarp();
                         if (lane == 0) mbar_arrive(bar(B_PUB_FULL + g));
