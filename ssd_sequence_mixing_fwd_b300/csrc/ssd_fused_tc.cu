@@ -900,17 +900,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int cc = 0; cc < 8; ++cc)
                             *reinterpret_cast<uint4 *>(hpbuf + swz(nrow, cc)) =
                                 make_uint4(hk[4 * cc], hk[4 * cc + 1], hk[4 * cc + 2], hk[4 * cc + 3]);
-                        // N = 256: rows 0-127 are published as soon as they are stored, so the
-                        // next block's first half need not wait for this block's second half
-                        if (hf == 0 && !last && (int64_t)blk != p.withhold) {
-                            if (leader) {
-                                if (npub >= 1) wait_bar(ctl, bar(B_PUB_DONE + g), (npub - 1) & 1);
-                                pubS[2 * g] = (int)sidx;
-                                pubS[2 * g + 1] = 2 * blk;
-                            }
+                        // N = 256 (chain-bound): each warp publishes its own 32 rows of each half
+                        // as soon as they are stored -- every lane fences its stores at GPU
+                        // scope, then one lane bumps the quarter's counter -- so the next block's
+                        // warp of the same quarter waits neither for the other warps nor for
+                        // this block's second half
+                        if (!last && (int64_t)blk != p.withhold) {
+                            fence_acq_rel_gpu();
                             __syncwarp();
-                            if (lane == 0) mbar_arrive(bar(B_PUB_FULL + g));
-                            ++npub;
+                            if (lane == 0)
+                                red_relaxed_add(p.flags + (sidx * 2 + (blk & 1)) * 4 * NS + q + 4 * hf, 32u);
                         }
                     }
                     }
@@ -920,7 +919,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         __syncwarp();
                         if (lane == 0) mbar_arrive(bar(B_HP_READY + g));
                     }
-                    if (!last && (int64_t)blk != p.withhold) {
+                    if (NS == 1 && !last && (int64_t)blk != p.withhold) {
                         // Hand the publication to this group's issuer warp, which makes the
                         // stores visible at GPU scope (fence) and bumps the counters, so these
                         // warps do not wait for the fence.  (h_prev is signalled first: the
