@@ -30,7 +30,8 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kTT = 16;        // tokens per shared-memory tile (chunk state)
-constexpr int kMaxAcc = 64;    // N*P / 256 accumulators per thread at most
+constexpr int kMaxAcc = 64;    // N*P / 256 accumulators per thread at most (chunk state)
+constexpr int kPassU = 8;      // chunks whose states are loaded together (state passing)
 constexpr int kRT = 32;        // output rows per block
 constexpr int kJT = 32;        // key (j) columns per tile
 constexpr int kMaxOut = 32;    // kRT*P / 256 outputs per thread at most
@@ -44,6 +45,18 @@ template <typename IO> __device__ __forceinline__ void st_io(IO *p, int64_t i, f
 template <> __device__ __forceinline__ void st_io<float>(float *p, int64_t i, float v) { p[i] = v; }
 template <> __device__ __forceinline__ void st_io<__nv_bfloat16>(__nv_bfloat16 *p, int64_t i, float v) {
     p[i] = __float2bfloat16_rn(v);
+}
+
+// e^x for the decay factors.  fp32 io keeps expf (the fp32 tolerance is 1e-5);
+// bf16 io (tolerance 2e-3) takes the hardware base-2 exponential, whose relative
+// error is ~2^-22 -- the inner loop of the diagonal-A output kernel evaluates one
+// decay per (i, j, n), and expf's range reduction made it the bulk of the time.
+template <typename IO> __device__ __forceinline__ float dexp(float x);
+template <> __device__ __forceinline__ float dexp<float>(float x) { return expf(x); }
+template <> __device__ __forceinline__ float dexp<__nv_bfloat16>(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x * 1.4426950408889634f));
+    return y;
 }
 
 // Inclusive prefix sum over the chunk of s_t = dt_t*A_h (scalar) or dt_t
@@ -67,7 +80,7 @@ __device__ __forceinline__ void chunk_prefix(const Problem &p, int bi, int h, in
     }
 }
 
-template <typename IO>
+template <typename IO, int ACC>
 __global__ void __launch_bounds__(kThreads) gen_chunk_state(Problem p, GenericWorkspace w) {
     extern __shared__ float smem[];
     const int c = blockIdx.x, h = blockIdx.y, bi = blockIdx.z, tid = threadIdx.x;
@@ -90,9 +103,9 @@ __global__ void __launch_bounds__(kThreads) gen_chunk_state(Problem p, GenericWo
     const int n0 = tid / P;
     const int nstep = kThreads / P;
     const int nacc = (N + nstep - 1) / nstep;
-    float acc[kMaxAcc];
+    float acc[ACC];                     // ACC >= nacc (N / nstep rounded up to a power of two)
 #pragma unroll
-    for (int a = 0; a < kMaxAcc; ++a) acc[a] = 0.f;
+    for (int a = 0; a < ACC; ++a) acc[a] = 0.f;
 
     for (int tt = 0; tt < L; tt += kTT) {
         for (int e = tid; e < kTT * N; e += kThreads) {
@@ -102,7 +115,7 @@ __global__ void __launch_bounds__(kThreads) gen_chunk_state(Problem p, GenericWo
                 const int64_t tok = (int64_t)bi * p.T + t0 + tt + k;
                 const float d = total - lcum[tt + k];
                 const float lw = (p.a_mode == SSD_A_SCALAR) ? d : p.A[(int64_t)h * N + n] * d;
-                v = ld_io(Bm, (tok * p.G + g) * N + n) * expf(lw);
+                v = ld_io(Bm, (tok * p.G + g) * N + n) * dexp<IO>(lw);
             }
             Bw[e] = v;
         }
@@ -121,7 +134,7 @@ __global__ void __launch_bounds__(kThreads) gen_chunk_state(Problem p, GenericWo
             for (int k = 0; k < kTT; ++k) {
                 const float xv = Xs[k * P + pcol];
 #pragma unroll
-                for (int a = 0; a < kMaxAcc; ++a) {
+                for (int a = 0; a < ACC; ++a) {
                     const int n = n0 + a * nstep;
                     if (a < nacc && n < N) acc[a] = fmaf(Bw[k * N + n], xv, acc[a]);
                 }
@@ -131,7 +144,7 @@ __global__ void __launch_bounds__(kThreads) gen_chunk_state(Problem p, GenericWo
     }
     float *out = w.states + (((int64_t)bi * p.H + h) * p.nc + c) * N * P;
 #pragma unroll
-    for (int a = 0; a < kMaxAcc; ++a) {
+    for (int a = 0; a < ACC; ++a) {
         const int n = n0 + a * nstep;
         if (a < nacc && n < N && n0 < nstep) out[(int64_t)n * P + pcol] = acc[a];
     }
@@ -148,11 +161,26 @@ __global__ void __launch_bounds__(kThreads) gen_state_passing(Problem p, Generic
     float *st = w.states + bh * p.nc * NP + o;
     const float *cs = w.chunk_sum + bh * p.nc;
     const float An = (p.a_mode == SSD_A_SCALAR) ? 1.f : p.A[(int64_t)h * p.N + n];
-    for (int64_t c = 0; c < p.nc; ++c) {
+    // the loads of kPassU chunks are issued together (the recurrence itself is a
+    // chain of FMAs; one load in flight per thread left the kernel latency-bound)
+    int64_t c = 0;
+    for (; c + kPassU <= p.nc; c += kPassU) {
+        float sv[kPassU], cv[kPassU];
+#pragma unroll
+        for (int u = 0; u < kPassU; ++u) {
+            sv[u] = st[(c + u) * NP];
+            cv[u] = cs[c + u];
+        }
+#pragma unroll
+        for (int u = 0; u < kPassU; ++u) {
+            st[(c + u) * NP] = hs;             // state entering chunk c + u
+            hs = fmaf(expf(An * cv[u]), hs, sv[u]);   // decay across the whole chunk
+        }
+    }
+    for (; c < p.nc; ++c) {
         const float s = st[c * NP];
-        st[c * NP] = hs;                       // state entering chunk c
-        const float a = expf(An * cs[c]);      // decay across the whole chunk
-        hs = fmaf(a, hs, s);
+        st[c * NP] = hs;
+        hs = fmaf(expf(An * cs[c]), hs, s);
     }
     if (p.final_state) p.final_state[bh * NP + o] = hs;
 }
@@ -181,10 +209,16 @@ __global__ void __launch_bounds__(kThreads) gen_chunk_output(Problem p, GenericW
     float *Xs = Bs + kJT * NS;                 // kJT x P
     float *Ss = Xs + kJT * P;                  // kRT x (kJT+1)
     float *Hs = Ss + kRT * (kJT + 1);          // kJT x P
+    // N x kRT: diagonal A, C_i[n] e^{A_n (cum_i - R)}; 16-byte aligned (read as float4)
+    float *CTs = smem + ((Hs + kJT * P - smem + 3) & ~3);
 
     chunk_prefix(p, bi, h, t0, L, lcum);
     for (int n = tid; n < N; n += kThreads)
         As[n] = (p.a_mode == SSD_A_SCALAR) ? 1.f : p.A[(int64_t)h * N + n];
+    // diagonal A: the largest |A_n| bounds the factors of the split decay below
+    float amax = 0.f;
+    if (p.a_mode != SSD_A_SCALAR)
+        for (int n = 0; n < N; ++n) amax = fmaxf(amax, fabsf(p.A[(int64_t)h * N + n]));
     for (int e = tid; e < kRT * N; e += kThreads) {
         const int r = e / N, n = e % N;
         float v = 0.f;
@@ -216,23 +250,68 @@ __global__ void __launch_bounds__(kThreads) gen_chunk_output(Problem p, GenericW
             Xs[e] = v;
         }
         __syncthreads();
-        for (int e = tid; e < kRT * kJT; e += kThreads) {
-            const int r = e / kJT, k = e % kJT;
-            const int i = i0 + r, j = j0 + k;
-            float v = 0.f;
-            if (j <= i && i < L) {
-                const float dlt = lcum[i] - lcum[j];
-                const float *cr = Cs + r * NS;
-                const float *br = Bs + k * NS;
-                if (p.a_mode == SSD_A_SCALAR) {
-                    float dot = 0.f;
-                    for (int n = 0; n < N; ++n) dot = fmaf(cr[n], br[n], dot);
-                    v = dot * expf(dlt);
-                } else {
-                    for (int n = 0; n < N; ++n) v = fmaf(cr[n] * br[n], expf(As[n] * dlt), v);
-                }
+        // Diagonal A: e^{A_n (cum_i - cum_j)} = e^{A_n (cum_i - R)} e^{A_n (R - cum_j)}.  With the
+        // first factor folded into C (stored transposed) and the second into B, the tile is a
+        // plain dot product over n, computed four rows per thread (no exponential inside).
+        // R = cum at the column tile's last token when the tile lies left of the rows (both
+        // factors <= 1); for the tile on the diagonal, R = cum at its middle row, taken only
+        // while amax * (half the tile's cum range) keeps the factors inside fp32 (< e^80);
+        // otherwise that tile is evaluated directly, one exponential per (i, j, n).
+        const int jl = min(j0 + kJT, L) - 1;
+        const bool below = jl < i0;
+        const float Rt = below ? lcum[jl] : lcum[min(i0 + kRT / 2, L) - 1];
+        const bool split = (p.a_mode != SSD_A_SCALAR) &&
+                           (below || amax * fmaxf(lcum[i_last] - Rt, Rt - lcum[j0]) < 80.f);
+        if (split) {
+            for (int e = tid; e < N * kRT; e += kThreads) {
+                const int n = e / kRT, r = e % kRT;
+                const int i = i0 + r;
+                CTs[n * kRT + r] = (i < L) ? Cs[r * NS + n] * dexp<IO>(As[n] * (lcum[i] - Rt)) : 0.f;
             }
-            Ss[r * (kJT + 1) + k] = v;
+            for (int e = tid; e < kJT * N; e += kThreads) {
+                const int k = e / N, n = e % N;
+                const int j = j0 + k;
+                Bs[k * NS + n] = (j < L) ? Bs[k * NS + n] * dexp<IO>(As[n] * (Rt - lcum[j])) : 0.f;
+            }
+            __syncthreads();
+            static_assert(kRT == 32 && kJT == 32 && kThreads == 256, "4 rows x 1 column per thread");
+            const int k = tid & 31, r4 = 4 * (tid >> 5);
+            const float *br = Bs + k * NS;
+            float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
+            for (int n = 0; n < N; ++n) {
+                const float4 c4 = *reinterpret_cast<const float4 *>(CTs + n * kRT + r4);
+                const float bv = br[n];
+                d0 = fmaf(c4.x, bv, d0);
+                d1 = fmaf(c4.y, bv, d1);
+                d2 = fmaf(c4.z, bv, d2);
+                d3 = fmaf(c4.w, bv, d3);
+            }
+            const int j = j0 + k;
+            const float dv[4] = {d0, d1, d2, d3};
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const int i = i0 + r4 + m;
+                Ss[(r4 + m) * (kJT + 1) + k] = (j <= i && i < L) ? dv[m] : 0.f;
+            }
+        } else {
+            for (int e = tid; e < kRT * kJT; e += kThreads) {
+                const int r = e / kJT, k = e % kJT;
+                const int i = i0 + r, j = j0 + k;
+                float v = 0.f;
+                if (j <= i && i < L) {
+                    const float dlt = lcum[i] - lcum[j];
+                    const float *cr = Cs + r * NS;
+                    const float *br = Bs + k * NS;
+                    if (p.a_mode == SSD_A_SCALAR) {
+                        float dot = 0.f;
+                        for (int n = 0; n < N; ++n) dot = fmaf(cr[n], br[n], dot);
+                        v = dot * dexp<IO>(dlt);
+                    } else {
+                        for (int n = 0; n < N; ++n) v = fmaf(cr[n] * br[n], dexp<IO>(As[n] * dlt), v);
+                    }
+                }
+                Ss[r * (kJT + 1) + k] = v;
+            }
         }
         __syncthreads();
         if (r0 < rstep) {
@@ -253,7 +332,7 @@ __global__ void __launch_bounds__(kThreads) gen_chunk_output(Problem p, GenericW
     for (int e = tid; e < kRT * N; e += kThreads) {
         const int r = e / N, n = e % N;
         const int i = i0 + r;
-        if (i < L) Cs[r * NS + n] *= expf(As[n] * lcum[i]);
+        if (i < L) Cs[r * NS + n] *= dexp<IO>(As[n] * lcum[i]);
     }
     const float *hprev = w.states + (((int64_t)bi * p.H + h) * p.nc + c) * N * P;
     for (int nb0 = 0; nb0 < N; nb0 += kJT) {
@@ -297,22 +376,36 @@ __global__ void __launch_bounds__(kThreads) gen_chunk_output(Problem p, GenericW
 size_t state_smem(const Problem &p) { return sizeof(float) * (p.Q + kTT * p.N + kTT * p.P); }
 size_t output_smem(const Problem &p) {
     const size_t NS = p.N + 1;
-    return sizeof(float) * (p.Q + p.N + kRT * NS + kJT * NS + kJT * p.P + kRT * (kJT + 1) + kJT * p.P);
+    return sizeof(float) * (p.Q + p.N + kRT * NS + kJT * NS + kJT * p.P + kRT * (kJT + 1) + kJT * p.P + 3 + p.N * kRT);
+}
+
+template <typename IO, int ACC>
+cudaError_t launch_state(const Problem &p, const GenericWorkspace &w, cudaStream_t s) {
+    const size_t sm1 = state_smem(p);
+    cudaError_t e;
+    if ((e = cudaFuncSetAttribute(gen_chunk_state<IO, ACC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)sm1)) != cudaSuccess)
+        return e;
+    dim3 g1((unsigned)p.nc, (unsigned)p.H, (unsigned)p.b);
+    gen_chunk_state<IO, ACC><<<g1, kThreads, sm1, s>>>(p, w);
+    return cudaGetLastError();
 }
 
 template <typename IO>
 cudaError_t launch_typed(const Problem &p, const GenericWorkspace &w, cudaStream_t s) {
-    const size_t sm1 = state_smem(p), sm3 = output_smem(p);
+    const size_t sm3 = output_smem(p);
     cudaError_t e;
-    if ((e = cudaFuncSetAttribute(gen_chunk_state<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)sm1)) != cudaSuccess)
-        return e;
     if ((e = cudaFuncSetAttribute(gen_chunk_output<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)sm3)) != cudaSuccess)
         return e;
-    dim3 g1((unsigned)p.nc, (unsigned)p.H, (unsigned)p.b);
-    gen_chunk_state<IO><<<g1, kThreads, sm1, s>>>(p, w);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // accumulators per thread of the chunk-state kernel: N / (threads / P), rounded up
+    const int64_t nacc = (p.N + (kThreads / p.P) - 1) / (kThreads / p.P);
+    if (nacc <= 4) e = launch_state<IO, 4>(p, w, s);
+    else if (nacc <= 8) e = launch_state<IO, 8>(p, w, s);
+    else if (nacc <= 16) e = launch_state<IO, 16>(p, w, s);
+    else if (nacc <= 32) e = launch_state<IO, 32>(p, w, s);
+    else e = launch_state<IO, kMaxAcc>(p, w, s);
+    if (e != cudaSuccess) return e;
     dim3 g2((unsigned)((p.N * p.P + kThreads - 1) / kThreads), (unsigned)p.H, (unsigned)p.b);
     gen_state_passing<<<g2, kThreads, 0, s>>>(p, w);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;

@@ -36,8 +36,11 @@ def _fused_ok(w):
         return False
 
 
-def test_withheld_state_reports_timeout_and_context_survives(cuda_device):
-    w = Workload("t", b=1, T=768, H=4, P=64, N=128, G=1, Q=128, D="none", seed=61)
+@pytest.mark.parametrize("N", [128, 256], ids=["n128_issuer_publishes", "n256_warps_publish"])
+def test_withheld_state_reports_timeout_and_context_survives(N, cuda_device):
+    # N = 128 publishes a block's state through the group's issuer warp; N = 256 has
+    # every warp publish its own rows of each half: both must time out cleanly
+    w = Workload("t", b=1, T=768, H=4, P=64, N=N, G=1, Q=128, D="none", seed=61)
     assert _fused_ok(w)
     inp = make_inputs(w)
     d = _dev(inp, cuda_device)

@@ -101,6 +101,21 @@ def test_small_cases_all_paths(name, w, cuda_device):
             compare(w, inp, y0, f0, drop_D=True)
 
 
+@pytest.mark.parametrize("dt_scale,dtype", [(1.0, "f32"), (1.0, "bf16"), (25.0, "bf16")],
+                         ids=["f32_split_tiles", "bf16_split_tiles", "bf16_large_decay_direct_tiles"])
+def test_diagonal_a_split_decay_tiles(dt_scale, dtype, cuda_device):
+    # The generic diagonal-A output kernel splits each tile's decay e^{A_n (cum_i - cum_j)}
+    # into a row and a column factor; a tile on the diagonal falls back to one exponential
+    # per (i, j, n) when the factors would leave fp32 range (dt scaled up 25x forces that).
+    # N = 50 puts the transposed factor buffer on a non-16-byte offset before its alignment.
+    w = Workload("t", b=2, T=200, H=3, P=64, N=50, G=1, Q=128, a_mode="diagonal", dtype=dtype,
+                 D="normal", init_std=0.1, seed=31)
+    inp = make_inputs(w)
+    inp["dt"] = inp["dt"] * dt_scale
+    y, fin = gpu_run(inp, w.Q, "generic")
+    compare(w, inp, y, fin)
+
+
 @pytest.mark.parametrize("name", ["tiny_fp32", "mamba2_130m", "diag_a"])
 def test_workload_full_parity(name, cuda_device):
     w = WORKLOADS[name]
