@@ -207,10 +207,11 @@ __global__ void __launch_bounds__(kThreads) gen_chunk_output(Problem p, GenericW
     float *Cs = As + N;                        // kRT x NS
     float *Bs = Cs + kRT * NS;                 // kJT x NS
     float *Xs = Bs + kJT * NS;                 // kJT x P
-    float *Ss = Xs + kJT * P;                  // kRT x (kJT+1)
-    float *Hs = Ss + kRT * (kJT + 1);          // kJT x P
-    // N x kRT: diagonal A, C_i[n] e^{A_n (cum_i - R)}; 16-byte aligned (read as float4)
-    float *CTs = smem + ((Hs + kJT * P - smem + 3) & ~3);
+    float *Hs = Xs + kJT * P;                  // kJT x P
+    // transposed buffers, read as float4 (16-byte aligned): S of a tile (ST[k][r]) and a
+    // decayed C (CT[n][r]: the row factor of a split diagonal-A tile, then e^{cum_i} C)
+    float *ST = smem + ((Hs + kJT * P - smem + 3) & ~3);   // kJT x kRT
+    float *CT = ST + kJT * kRT;                            // N x kRT
 
     chunk_prefix(p, bi, h, t0, L, lcum);
     for (int n = tid; n < N; n += kThreads)
@@ -227,13 +228,35 @@ __global__ void __launch_bounds__(kThreads) gen_chunk_output(Problem p, GenericW
     }
     __syncthreads();
 
+    // Each thread owns column pcol of y and the nout consecutive rows from rbase, so that a
+    // k step of a product reads one value of its column and the rows' values as float4.
     const int pcol = tid % P;
-    const int r0 = tid / P;
-    const int rstep = kThreads / P;            // >= 1 since P <= 256
-    const int nout = (kRT + rstep - 1) / rstep;
+    const int rblocks = kThreads / P;          // >= 1 since P <= 256
+    const int nout = rblocks >= kRT ? 1 : kRT / rblocks;
+    const int rbase = (tid / P) * nout;
+    const bool active = rbase < kRT;
     float acc[kMaxOut];
 #pragma unroll
     for (int a = 0; a < kMaxOut; ++a) acc[a] = 0.f;
+    // acc[a] += v[a] * x for the thread's rows, v = the nout values at vk (16-byte aligned)
+    auto accumulate = [&](const float *vk, float x) {
+        if (nout >= 4) {
+#pragma unroll
+            for (int a = 0; a < kMaxOut; a += 4) {
+                if (a < nout) {
+                    const float4 v4 = *reinterpret_cast<const float4 *>(vk + a);
+                    acc[a] = fmaf(v4.x, x, acc[a]);
+                    acc[a + 1] = fmaf(v4.y, x, acc[a + 1]);
+                    acc[a + 2] = fmaf(v4.z, x, acc[a + 2]);
+                    acc[a + 3] = fmaf(v4.w, x, acc[a + 3]);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+                if (a < nout) acc[a] = fmaf(vk[a], x, acc[a]);
+        }
+    };
 
     const int i_last = min(i0 + kRT, L) - 1;
     for (int j0 = 0; j0 <= i_last; j0 += kJT) {
@@ -251,8 +274,8 @@ __global__ void __launch_bounds__(kThreads) gen_chunk_output(Problem p, GenericW
         }
         __syncthreads();
         // Diagonal A: e^{A_n (cum_i - cum_j)} = e^{A_n (cum_i - R)} e^{A_n (R - cum_j)}.  With the
-        // first factor folded into C (stored transposed) and the second into B, the tile is a
-        // plain dot product over n, computed four rows per thread (no exponential inside).
+        // first factor folded into C (transposed, CT) and the second into B, the tile is a plain
+        // dot product over n, computed four rows per thread (no exponential inside).
         // R = cum at the column tile's last token when the tile lies left of the rows (both
         // factors <= 1); for the tile on the diagonal, R = cum at its middle row, taken only
         // while amax * (half the tile's cum range) keeps the factors inside fp32 (< e^80);
@@ -266,7 +289,7 @@ __global__ void __launch_bounds__(kThreads) gen_chunk_output(Problem p, GenericW
             for (int e = tid; e < N * kRT; e += kThreads) {
                 const int n = e / kRT, r = e % kRT;
                 const int i = i0 + r;
-                CTs[n * kRT + r] = (i < L) ? Cs[r * NS + n] * dexp<IO>(As[n] * (lcum[i] - Rt)) : 0.f;
+                CT[n * kRT + r] = (i < L) ? Cs[r * NS + n] * dexp<IO>(As[n] * (lcum[i] - Rt)) : 0.f;
             }
             for (int e = tid; e < kJT * N; e += kThreads) {
                 const int k = e / N, n = e % N;
@@ -279,23 +302,20 @@ __global__ void __launch_bounds__(kThreads) gen_chunk_output(Problem p, GenericW
             const float *br = Bs + k * NS;
             float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
             for (int n = 0; n < N; ++n) {
-                const float4 c4 = *reinterpret_cast<const float4 *>(CTs + n * kRT + r4);
+                const float4 c4 = *reinterpret_cast<const float4 *>(CT + n * kRT + r4);
                 const float bv = br[n];
                 d0 = fmaf(c4.x, bv, d0);
                 d1 = fmaf(c4.y, bv, d1);
                 d2 = fmaf(c4.z, bv, d2);
                 d3 = fmaf(c4.w, bv, d3);
             }
-            const int j = j0 + k;
-            const float dv[4] = {d0, d1, d2, d3};
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const int i = i0 + r4 + m;
-                Ss[(r4 + m) * (kJT + 1) + k] = (j <= i && i < L) ? dv[m] : 0.f;
-            }
+            const int j = j0 + k, i = i0 + r4;
+            *reinterpret_cast<float4 *>(ST + k * kRT + r4) =
+                make_float4((j <= i && i < L) ? d0 : 0.f, (j <= i + 1 && i + 1 < L) ? d1 : 0.f,
+                            (j <= i + 2 && i + 2 < L) ? d2 : 0.f, (j <= i + 3 && i + 3 < L) ? d3 : 0.f);
         } else {
             for (int e = tid; e < kRT * kJT; e += kThreads) {
-                const int r = e / kJT, k = e % kJT;
+                const int r = e % kRT, k = e / kRT;
                 const int i = i0 + r, j = j0 + k;
                 float v = 0.f;
                 if (j <= i && i < L) {
@@ -310,29 +330,21 @@ __global__ void __launch_bounds__(kThreads) gen_chunk_output(Problem p, GenericW
                         for (int n = 0; n < N; ++n) v = fmaf(cr[n] * br[n], dexp<IO>(As[n] * dlt), v);
                     }
                 }
-                Ss[r * (kJT + 1) + k] = v;
+                ST[k * kRT + r] = v;
             }
         }
         __syncthreads();
-        if (r0 < rstep) {
-#pragma unroll
-            for (int a = 0; a < kMaxOut; ++a) {
-                const int r = r0 + a * rstep;
-                if (a < nout && r < kRT) {
-                    float s = acc[a];
-                    for (int k = 0; k < kJT; ++k) s = fmaf(Ss[r * (kJT + 1) + k], Xs[k * P + pcol], s);
-                    acc[a] = s;
-                }
-            }
-        }
+        // Y_diag += S X (columns past the sequence end have X = 0)
+        if (active)
+            for (int k = 0; k < kJT; ++k) accumulate(ST + k * kRT + rbase, Xs[k * P + pcol]);
         __syncthreads();
     }
 
-    // Off-diagonal blocks: exp(cum_i) C_i^T h_{c-1}; fold the decay into C.
-    for (int e = tid; e < kRT * N; e += kThreads) {
-        const int r = e / N, n = e % N;
+    // Off-diagonal blocks: e^{cum_i} C_i^T h_{c-1}, with the decay folded into C (transposed)
+    for (int e = tid; e < N * kRT; e += kThreads) {
+        const int n = e / kRT, r = e % kRT;
         const int i = i0 + r;
-        if (i < L) Cs[r * NS + n] *= dexp<IO>(As[n] * lcum[i]);
+        CT[n * kRT + r] = (i < L) ? Cs[r * NS + n] * dexp<IO>(As[n] * lcum[i]) : 0.f;
     }
     const float *hprev = w.states + (((int64_t)bi * p.H + h) * p.nc + c) * N * P;
     for (int nb0 = 0; nb0 < N; nb0 += kJT) {
@@ -343,27 +355,17 @@ __global__ void __launch_bounds__(kThreads) gen_chunk_output(Problem p, GenericW
         }
         __syncthreads();
         const int kmax = min(kJT, N - nb0);
-        if (r0 < rstep) {
-#pragma unroll
-            for (int a = 0; a < kMaxOut; ++a) {
-                const int r = r0 + a * rstep;
-                if (a < nout && r < kRT) {
-                    float s = acc[a];
-                    for (int k = 0; k < kmax; ++k) s = fmaf(Cs[r * NS + nb0 + k], Hs[k * P + pcol], s);
-                    acc[a] = s;
-                }
-            }
-        }
+        if (active)
+            for (int k = 0; k < kmax; ++k) accumulate(CT + (nb0 + k) * kRT + rbase, Hs[k * P + pcol]);
     }
 
     IO *Y = static_cast<IO *>(p.y);
     const float Dh = p.D ? p.D[h] : 0.f;
-    if (r0 < rstep) {
+    if (active) {
 #pragma unroll
         for (int a = 0; a < kMaxOut; ++a) {
-            const int r = r0 + a * rstep;
-            const int i = i0 + r;
-            if (a < nout && r < kRT && i < L) {
+            const int i = i0 + rbase + a;
+            if (a < nout && i < L) {
                 const int64_t off = (((int64_t)bi * p.T + t0 + i) * p.H + h) * P + pcol;
                 float v = acc[a];
                 if (p.D) v = fmaf(Dh, ld_io(X, off), v);
@@ -376,7 +378,7 @@ __global__ void __launch_bounds__(kThreads) gen_chunk_output(Problem p, GenericW
 size_t state_smem(const Problem &p) { return sizeof(float) * (p.Q + kTT * p.N + kTT * p.P); }
 size_t output_smem(const Problem &p) {
     const size_t NS = p.N + 1;
-    return sizeof(float) * (p.Q + p.N + kRT * NS + kJT * NS + kJT * p.P + kRT * (kJT + 1) + kJT * p.P + 3 + p.N * kRT);
+    return sizeof(float) * (p.Q + p.N + kRT * NS + kJT * NS + 2 * kJT * p.P + 3 + kJT * kRT + p.N * kRT);
 }
 
 template <typename IO, int ACC>
