@@ -91,19 +91,20 @@ __global__ void __launch_bounds__(kThreads) gen_chunk_state(Problem p, GenericWo
     const IO *X = static_cast<const IO *>(p.x);
     const IO *Bm = static_cast<const IO *>(p.B);
 
+    const int NW = (N + 3) & ~3;        // Bw row stride (float4 rows)
     float *lcum = smem;                 // Q
-    float *Bw = lcum + p.Q;             // kTT x N
-    float *Xs = Bw + kTT * N;           // kTT x P
+    float *Bw = smem + ((p.Q + 3) & ~3);   // kTT x NW, 16-byte aligned rows
+    float *Xs = Bw + kTT * NW;          // kTT x P
 
     chunk_prefix(p, bi, h, t0, L, lcum);
     const float total = lcum[L - 1];
     if (tid == 0) w.chunk_sum[((int64_t)bi * p.H + h) * p.nc + c] = total;
 
+    // thread: column pcol of the state and the ACC consecutive state rows from nbase
+    // (ACC >= N / (threads / P), a power of two), read from Bw as float4
     const int pcol = tid % P;
-    const int n0 = tid / P;
-    const int nstep = kThreads / P;
-    const int nacc = (N + nstep - 1) / nstep;
-    float acc[ACC];                     // ACC >= nacc (N / nstep rounded up to a power of two)
+    const int nbase = (tid / P) * ACC;
+    float acc[ACC];
 #pragma unroll
     for (int a = 0; a < ACC; ++a) acc[a] = 0.f;
 
@@ -117,7 +118,7 @@ __global__ void __launch_bounds__(kThreads) gen_chunk_state(Problem p, GenericWo
                 const float lw = (p.a_mode == SSD_A_SCALAR) ? d : p.A[(int64_t)h * N + n] * d;
                 v = ld_io(Bm, (tok * p.G + g) * N + n) * dexp<IO>(lw);
             }
-            Bw[e] = v;
+            Bw[k * NW + n] = v;
         }
         for (int e = tid; e < kTT * P; e += kThreads) {
             const int k = e / P, pp = e % P;
@@ -129,14 +130,20 @@ __global__ void __launch_bounds__(kThreads) gen_chunk_state(Problem p, GenericWo
             Xs[e] = v;
         }
         __syncthreads();
-        if (n0 < nstep) {
+        if (nbase < N) {
 #pragma unroll 4
             for (int k = 0; k < kTT; ++k) {
                 const float xv = Xs[k * P + pcol];
+                const float *bk = Bw + k * NW + nbase;
 #pragma unroll
-                for (int a = 0; a < ACC; ++a) {
-                    const int n = n0 + a * nstep;
-                    if (a < nacc && n < N) acc[a] = fmaf(Bw[k * N + n], xv, acc[a]);
+                for (int a = 0; a < ACC; a += 4) {
+                    if (nbase + a < NW) {
+                        const float4 b4 = *reinterpret_cast<const float4 *>(bk + a);
+                        acc[a] = fmaf(b4.x, xv, acc[a]);
+                        acc[a + 1] = fmaf(b4.y, xv, acc[a + 1]);
+                        acc[a + 2] = fmaf(b4.z, xv, acc[a + 2]);
+                        acc[a + 3] = fmaf(b4.w, xv, acc[a + 3]);
+                    }
                 }
             }
         }
@@ -145,8 +152,8 @@ __global__ void __launch_bounds__(kThreads) gen_chunk_state(Problem p, GenericWo
     float *out = w.states + (((int64_t)bi * p.H + h) * p.nc + c) * N * P;
 #pragma unroll
     for (int a = 0; a < ACC; ++a) {
-        const int n = n0 + a * nstep;
-        if (a < nacc && n < N && n0 < nstep) out[(int64_t)n * P + pcol] = acc[a];
+        const int n = nbase + a;
+        if (n < N) out[(int64_t)n * P + pcol] = acc[a];
     }
 }
 
@@ -375,7 +382,7 @@ __global__ void __launch_bounds__(kThreads) gen_chunk_output(Problem p, GenericW
     }
 }
 
-size_t state_smem(const Problem &p) { return sizeof(float) * (p.Q + kTT * p.N + kTT * p.P); }
+size_t state_smem(const Problem &p) { return sizeof(float) * (((p.Q + 3) & ~3) + kTT * ((p.N + 3) & ~3) + kTT * p.P); }
 size_t output_smem(const Problem &p) {
     const size_t NS = p.N + 1;
     return sizeof(float) * (p.Q + p.N + kRT * NS + kJT * NS + 2 * kJT * p.P + 3 + kJT * kRT + p.N * kRT);
