@@ -204,7 +204,7 @@ def run_ours(args, w):
     host = make_inputs(w, seed=w.seed + rank)
     pinned = {k: (None if v is None else v.pin_memory()) for k, v in host.items()}
     d = {k: (None if v is None else v.to(dev)) for k, v in host.items()}
-    dims = ssd.make_dims(w.b, w.T, w.H, w.P, w.N, w.G, w.Q, w.a_mode, w.dtype)
+    dims = ssd.make_dims(w.b, w.T, w.H, w.P, w.N, w.G, w.Q, w.a_mode, w.dtype, path=args.path)
     path = ssd.ssd_fwd_path(dims)
     ws = torch.empty(max(ssd.ssd_fwd_workspace_size(dims), 256), device=dev, dtype=torch.uint8)
     y = torch.empty_like(d["x"])
@@ -214,7 +214,7 @@ def run_ours(args, w):
 
     # the public call, with its arguments marshalled once (same buffers every step)
     step = ssd.PreparedCall(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["init_state"], chunk_Q=w.Q,
-                            y=y, final_state=fin, workspace=ws, stream=stream)
+                            path=args.path, y=y, final_state=fin, workspace=ws, stream=stream)
 
     for _ in range(args.warmup):
         flush.fill_(1.0)
@@ -273,8 +273,8 @@ def run_ours(args, w):
         yy = y if sidx == 0 else torch.empty_like(y)
         ff = fin if sidx == 0 else torch.empty_like(fin)
         call = step if sidx == 0 else ssd.PreparedCall(dd["x"], dd["dt"], dd["A"], dd["B"], dd["C"], dd["D"],
-                                                       dd["init_state"], chunk_Q=w.Q, y=yy, final_state=ff,
-                                                       workspace=ws, stream=stream)
+                                                       dd["init_state"], chunk_Q=w.Q, path=args.path, y=yy,
+                                                       final_state=ff, workspace=ws, stream=stream)
         sets.append(dict(d=dd, y=yy, fin=ff, call=call,
                          y_host=torch.empty(y.shape, dtype=y.dtype, pin_memory=True),
                          f_host=torch.empty(fin.shape, dtype=fin.dtype, pin_memory=True),
@@ -396,6 +396,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="mamba2_2p7b", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--path", default="auto", choices=["auto", "generic", "tcgen05"],
+                    help="kernel path (auto: the fused tcgen05 kernel where it applies)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
     ap.add_argument("--batch", type=int, default=None,

@@ -20,7 +20,8 @@
 //
 // In the diagonal-A variant the decay of state dim n between tokens j <= i is
 // exp(A_{h,n} (S_i - S_j)) with S the chunk prefix sum of dt, so the mask is a
-// sum over n and is formed inside the n loop.
+// sum over n.  In both variants the output kernel splits each tile's decay into
+// a row and a column factor, so that the (i, j) products are plain dot products.
 #include <cuda_bf16.h>
 
 #include "ssd_internal.cuh"
@@ -223,8 +224,9 @@ __global__ void __launch_bounds__(kThreads) gen_chunk_output(Problem p, GenericW
     chunk_prefix(p, bi, h, t0, L, lcum);
     for (int n = tid; n < N; n += kThreads)
         As[n] = (p.a_mode == SSD_A_SCALAR) ? 1.f : p.A[(int64_t)h * N + n];
-    // diagonal A: the largest |A_n| bounds the factors of the split decay below
-    float amax = 0.f;
+    // the largest |A_n| bounds the factors of the split decay below (scalar A: its cum
+    // already carries A, and As = 1)
+    float amax = (p.a_mode == SSD_A_SCALAR) ? 1.f : 0.f;
     if (p.a_mode != SSD_A_SCALAR)
         for (int n = 0; n < N; ++n) amax = fmaxf(amax, fabsf(p.A[(int64_t)h * N + n]));
     for (int e = tid; e < kRT * N; e += kThreads) {
@@ -280,18 +282,17 @@ __global__ void __launch_bounds__(kThreads) gen_chunk_output(Problem p, GenericW
             Xs[e] = v;
         }
         __syncthreads();
-        // Diagonal A: e^{A_n (cum_i - cum_j)} = e^{A_n (cum_i - R)} e^{A_n (R - cum_j)}.  With the
-        // first factor folded into C (transposed, CT) and the second into B, the tile is a plain
-        // dot product over n, computed four rows per thread (no exponential inside).
-        // R = cum at the column tile's last token when the tile lies left of the rows (both
-        // factors <= 1); for the tile on the diagonal, R = cum at its middle row, taken only
-        // while amax * (half the tile's cum range) keeps the factors inside fp32 (< e^80);
-        // otherwise that tile is evaluated directly, one exponential per (i, j, n).
+        // e^{A_n (cum_i - cum_j)} = e^{A_n (cum_i - R)} e^{A_n (R - cum_j)} (scalar A: A_n = 1 and
+        // cum carries A).  With the first factor folded into C (transposed, CT) and the second
+        // into B, the tile is a plain dot product over n, computed four rows per thread (no
+        // exponential inside).  R = cum at the column tile's last token when the tile lies left
+        // of the rows (both factors <= 1); for the tile on the diagonal, R = cum at its middle
+        // row, taken only while amax * (half the tile's cum range) keeps the factors inside
+        // fp32 (< e^80); otherwise that tile is evaluated directly.
         const int jl = min(j0 + kJT, L) - 1;
         const bool below = jl < i0;
         const float Rt = below ? lcum[jl] : lcum[min(i0 + kRT / 2, L) - 1];
-        const bool split = (p.a_mode != SSD_A_SCALAR) &&
-                           (below || amax * fmaxf(lcum[i_last] - Rt, Rt - lcum[j0]) < 80.f);
+        const bool split = below || amax * fmaxf(fabsf(lcum[i_last] - Rt), fabsf(Rt - lcum[j0])) < 80.f;
         if (split) {
             for (int e = tid; e < N * kRT; e += kThreads) {
                 const int n = e / kRT, r = e % kRT;
