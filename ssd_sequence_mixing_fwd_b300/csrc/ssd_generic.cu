@@ -48,6 +48,46 @@ template <> __device__ __forceinline__ void st_io<__nv_bfloat16>(__nv_bfloat16 *
     p[i] = __float2bfloat16_rn(v);
 }
 
+// dst[k * ds + c] = src[base + k * rs + c] for k < rows, c < cols (0 for k >= valid), as
+// 16-byte loads when base, rs and cols allow it (8 bf16 or 4 fp32 per load; the pointers
+// of the ABI are 16-byte aligned), else element by element.  All threads of the block.
+template <typename IO>
+__device__ __forceinline__ void load_tile(float *dst, int ds, const IO *src, int64_t base, int64_t rs, int rows,
+                                          int valid, int cols) {
+    constexpr int V = 16 / (int)sizeof(IO);
+    if ((cols % V) == 0 && (base % V) == 0 && (rs % V) == 0) {
+        const int cv = cols / V;
+        for (int e = threadIdx.x; e < rows * cv; e += blockDim.x) {
+            const int k = e / cv, c = (e % cv) * V;
+            float *d = dst + k * ds + c;
+            if (k < valid) {
+                const uint4 u = *reinterpret_cast<const uint4 *>(src + base + k * rs + c);
+                if constexpr (sizeof(IO) == 2) {
+                    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        d[2 * q] = __uint_as_float(w[q] << 16);
+                        d[2 * q + 1] = __uint_as_float(w[q] & 0xffff0000u);
+                    }
+                } else {
+                    d[0] = __uint_as_float(u.x);
+                    d[1] = __uint_as_float(u.y);
+                    d[2] = __uint_as_float(u.z);
+                    d[3] = __uint_as_float(u.w);
+                }
+            } else {
+#pragma unroll
+                for (int q = 0; q < V; ++q) d[q] = 0.f;
+            }
+        }
+    } else {
+        for (int e = threadIdx.x; e < rows * cols; e += blockDim.x) {
+            const int k = e / cols, c = e % cols;
+            dst[k * ds + c] = (k < valid) ? ld_io(src, base + k * rs + c) : 0.f;
+        }
+    }
+}
+
 // e^x for the decay factors.  fp32 io keeps expf (the fp32 tolerance is 1e-5);
 // bf16 io (tolerance 2e-3) takes the hardware base-2 exponential, whose relative
 // error is ~2^-22 -- the inner loop of the diagonal-A output kernel evaluates one
@@ -121,15 +161,7 @@ __global__ void __launch_bounds__(kThreads) gen_chunk_state(Problem p, GenericWo
             }
             Bw[k * NW + n] = v;
         }
-        for (int e = tid; e < kTT * P; e += kThreads) {
-            const int k = e / P, pp = e % P;
-            float v = 0.f;
-            if (tt + k < L) {
-                const int64_t tok = (int64_t)bi * p.T + t0 + tt + k;
-                v = ld_io(X, (tok * p.H + h) * P + pp);
-            }
-            Xs[e] = v;
-        }
+        load_tile(Xs, P, X, (((int64_t)bi * p.T + t0 + tt) * p.H + h) * P, (int64_t)p.H * P, kTT, L - tt, P);
         __syncthreads();
         if (nbase < N) {
 #pragma unroll 4
@@ -229,12 +261,7 @@ __global__ void __launch_bounds__(kThreads) gen_chunk_output(Problem p, GenericW
     float amax = (p.a_mode == SSD_A_SCALAR) ? 1.f : 0.f;
     if (p.a_mode != SSD_A_SCALAR)
         for (int n = 0; n < N; ++n) amax = fmaxf(amax, fabsf(p.A[(int64_t)h * N + n]));
-    for (int e = tid; e < kRT * N; e += kThreads) {
-        const int r = e / N, n = e % N;
-        float v = 0.f;
-        if (i0 + r < L) v = ld_io(Cm, (((int64_t)bi * p.T + t0 + i0 + r) * p.G + g) * N + n);
-        Cs[r * NS + n] = v;
-    }
+    load_tile(Cs, NS, Cm, (((int64_t)bi * p.T + t0 + i0) * p.G + g) * N, (int64_t)p.G * N, kRT, L - i0, N);
     __syncthreads();
 
     // Each thread owns column pcol of y and the nout consecutive rows from rbase, so that a
@@ -269,18 +296,8 @@ __global__ void __launch_bounds__(kThreads) gen_chunk_output(Problem p, GenericW
 
     const int i_last = min(i0 + kRT, L) - 1;
     for (int j0 = 0; j0 <= i_last; j0 += kJT) {
-        for (int e = tid; e < kJT * N; e += kThreads) {
-            const int k = e / N, n = e % N;
-            float v = 0.f;
-            if (j0 + k < L) v = ld_io(Bm, (((int64_t)bi * p.T + t0 + j0 + k) * p.G + g) * N + n);
-            Bs[k * NS + n] = v;
-        }
-        for (int e = tid; e < kJT * P; e += kThreads) {
-            const int k = e / P, pp = e % P;
-            float v = 0.f;
-            if (j0 + k < L) v = ld_io(X, (((int64_t)bi * p.T + t0 + j0 + k) * p.H + h) * P + pp);
-            Xs[e] = v;
-        }
+        load_tile(Bs, NS, Bm, (((int64_t)bi * p.T + t0 + j0) * p.G + g) * N, (int64_t)p.G * N, kJT, L - j0, N);
+        load_tile(Xs, P, X, (((int64_t)bi * p.T + t0 + j0) * p.H + h) * P, (int64_t)p.H * P, kJT, L - j0, P);
         __syncthreads();
         // e^{A_n (cum_i - cum_j)} = e^{A_n (cum_i - R)} e^{A_n (R - cum_j)} (scalar A: A_n = 1 and
         // cum carries A).  With the first factor folded into C (transposed, CT) and the second
@@ -357,10 +374,7 @@ __global__ void __launch_bounds__(kThreads) gen_chunk_output(Problem p, GenericW
     const float *hprev = w.states + (((int64_t)bi * p.H + h) * p.nc + c) * N * P;
     for (int nb0 = 0; nb0 < N; nb0 += kJT) {
         __syncthreads();
-        for (int e = tid; e < kJT * P; e += kThreads) {
-            const int k = e / P;
-            Hs[e] = (nb0 + k < N) ? hprev[(int64_t)(nb0 + k) * P + (e % P)] : 0.f;
-        }
+        load_tile(Hs, P, hprev, (int64_t)nb0 * P, (int64_t)P, kJT, N - nb0, P);
         __syncthreads();
         const int kmax = min(kJT, N - nb0);
         if (active)
