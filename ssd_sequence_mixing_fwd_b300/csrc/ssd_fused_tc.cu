@@ -337,6 +337,28 @@ __device__ __forceinline__ void decode_item(const FusedParams &p, int t, int &bi
     hgi = rem - bi * p.HG;
 }
 
+// C and B of a stage, bf16 -> fp16 in place: row r of each of the nbox boxes.  Chunk
+// c ^ (r & 7): eight consecutive rows touch eight different 16-byte bank groups (walking
+// chunk c of every row would put a quarter warp on the same four banks).
+__device__ __noinline__ void convert_stage_rows(unsigned char *base, int nbox, int r) {
+    const uint32_t rx = (uint32_t)(r & 7) * 16u;
+#pragma unroll 1
+    for (int bx = 0; bx < nbox; ++bx) {
+        unsigned char *row = base + bx * kBox + r * 128;
+        uint4 u[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) u[c] = *reinterpret_cast<const uint4 *>(row + ((16u * c) ^ rx));
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            u[c].x = bf2_to_h2(u[c].x);
+            u[c].y = bf2_to_h2(u[c].y);
+            u[c].z = bf2_to_h2(u[c].z);
+            u[c].w = bf2_to_h2(u[c].w);
+            *reinterpret_cast<uint4 *>(row + ((16u * c) ^ rx)) = u[c];
+        }
+    }
+}
+
 template <int NS>
 __global__ void __launch_bounds__(kThreads, 1)
     ssd_fused_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_B,
@@ -644,6 +666,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         int it = 0, flat = 0, hcnt = 0, npub = 0;
         bool ok = true;
+        bool conv_ahead = false;                // this warp converted the current stage's rows ahead
         for (;; ++it) {
             const int st = it % NST;
             if (!(ok = wait_bar(ctl, bar(B_CB_FULL + st), (it / NST) & 1))) break;
@@ -658,27 +681,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // group that owns the item's first head does it: that group has no Y_off
             // of the previous item outstanding, so C B^T of this item never waits on
             // the other group's state chain.
-            if (j0 == 0) {
-                unsigned char *base = smem + kOffStage + st * kStage;
-                // chunk c ^ (r & 7): eight consecutive rows touch eight different 16-byte
-                // bank groups (walking chunk c of every row would put a quarter warp on
-                // the same four banks)
-                const uint32_t rx = (uint32_t)(r & 7) * 16u;
-#pragma unroll 1
-                for (int bx = 0; bx < 4 * NS; ++bx) {
-                    unsigned char *row = base + bx * kBox + r * 128;
-                    uint4 u[8];
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) u[c] = *reinterpret_cast<const uint4 *>(row + ((16u * c) ^ rx));
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        u[c].x = bf2_to_h2(u[c].x);
-                        u[c].y = bf2_to_h2(u[c].y);
-                        u[c].z = bf2_to_h2(u[c].z);
-                        u[c].w = bf2_to_h2(u[c].w);
-                        *reinterpret_cast<uint4 *>(row + ((16u * c) ^ rx)) = u[c];
-                    }
-                }
+            // (N = 128: a warp that found this stage already landed during its last head of the
+            // previous item has converted its rows then, while it waited for C h_prev)
+            if (j0 == 0 && !conv_ahead) {
+                convert_stage_rows(smem + kOffStage + st * kStage, 4 * NS, r);
                 if (!p.dt_tma) {
                     // dt tile by thread loads (rows past the sequence end are zero)
                     float *tile = dtT + st * (kBlk * kMaxK);
@@ -689,6 +695,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(B_CB_CONV + st));
             }
+            conv_ahead = false;
             const int my_count = (k - j0 + NG - 1) / NG;
             // A (log2 units) and D of the item's heads: written by the producer with the stage
             const float *adS = reinterpret_cast<const float *>(smem + kOffAD) + st * (2 * kMaxK);
@@ -936,6 +943,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ++npub;
                     }
 
+                }
+                // N = 128: in the group's last head of the item, while C h_prev runs, convert the
+                // next item's C/B if this group owns that item's first head and its tiles have
+                // landed (a non-blocking test; otherwise the conversion waits for the item start)
+                if constexpr (NS == 1) {
+                    if (s == my_count - 1 && p.dt_tma && (flat + k) % NG == g) {
+                        const int st2 = (it + 1) % NST;
+                        const bool landed = __shfl_sync(0xffffffffu,
+                                                        lane == 0 ? (int)mbar_test(bar(B_CB_FULL + st2), ((it + 1) / NST) & 1) : 0, 0);
+                        if (landed && itemS[st2] >= 0) {
+                            convert_stage_rows(smem + kOffStage + st2 * kStage, 4 * NS, r);
+                            fence_async_smem();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(bar(B_CB_CONV + st2));
+                            conv_ahead = true;
+                        }
+                    }
                 }
                 // (5) epilogue: y = Y_diag + 2^cum_i Y_off + D x  ->  bf16 into the W buffer, TMA store
                 if (!(ok = wait_bar(ctl, bar(B_YO_FULL + g), hcnt & 1))) break;
