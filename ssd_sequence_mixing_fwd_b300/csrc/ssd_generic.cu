@@ -247,22 +247,23 @@ __global__ void __launch_bounds__(kThreads) gen_chunk_output(Problem p, GenericW
     float *Cs = As + N;                        // kRT x NS
     float *Bs = Cs + kRT * NS;                 // kJT x NS
     float *Xs = Bs + kJT * NS;                 // kJT x P
-    float *Hs = Xs + kJT * P;                  // kJT x P
+    // kJT x P tile of h_{c-1}: only after the column tiles, in the B and X tiles' space
+    // (kJT * (NS + P) >= kJT * P floats)
+    float *Hs = Bs;
     // transposed buffers, read as float4 (16-byte aligned): S of a tile (ST[k][r]) and a
     // decayed C (CT[n][r]: the row factor of a split diagonal-A tile, then e^{cum_i} C)
-    float *ST = smem + ((Hs + kJT * P - smem + 3) & ~3);   // kJT x kRT
+    float *ST = smem + ((Xs + kJT * P - smem + 3) & ~3);   // kJT x kRT
     float *CT = ST + kJT * kRT;                            // N x kRT
 
     chunk_prefix(p, bi, h, t0, L, lcum);
     for (int n = tid; n < N; n += kThreads)
         As[n] = (p.a_mode == SSD_A_SCALAR) ? 1.f : p.A[(int64_t)h * N + n];
-    // the largest |A_n| bounds the factors of the split decay below (scalar A: its cum
-    // already carries A, and As = 1)
-    float amax = (p.a_mode == SSD_A_SCALAR) ? 1.f : 0.f;
-    if (p.a_mode != SSD_A_SCALAR)
-        for (int n = 0; n < N; ++n) amax = fmaxf(amax, fabsf(p.A[(int64_t)h * N + n]));
     load_tile(Cs, NS, Cm, (((int64_t)bi * p.T + t0 + i0) * p.G + g) * N, (int64_t)p.G * N, kRT, L - i0, N);
     __syncthreads();
+    // the largest |A_n| bounds the factors of the split decay below (scalar A: its cum
+    // already carries A, and As = 1)
+    float amax = 0.f;
+    for (int n = 0; n < N; ++n) amax = fmaxf(amax, fabsf(As[n]));
 
     // Each thread owns column pcol of y and the nout consecutive rows from rbase, so that a
     // k step of a product reads one value of its column and the rows' values as float4.
@@ -400,7 +401,7 @@ __global__ void __launch_bounds__(kThreads) gen_chunk_output(Problem p, GenericW
 size_t state_smem(const Problem &p) { return sizeof(float) * (((p.Q + 3) & ~3) + kTT * ((p.N + 3) & ~3) + kTT * p.P); }
 size_t output_smem(const Problem &p) {
     const size_t NS = p.N + 1;
-    return sizeof(float) * (p.Q + p.N + kRT * NS + kJT * NS + 2 * kJT * p.P + 3 + kJT * kRT + p.N * kRT);
+    return sizeof(float) * (p.Q + p.N + kRT * NS + kJT * NS + kJT * p.P + 3 + kJT * kRT + p.N * kRT);
 }
 
 template <typename IO, int ACC>
