@@ -159,6 +159,57 @@ class ClockSampler:
                                    default=None)}
 
 
+def workload_config(w, world):
+    """The `config` object of the JSON line: the workload, the same in both arms."""
+    return {"workload": w.name, "b": w.b, "T": w.T, "H": w.H, "P": w.P, "N": w.N, "G": w.G, "Q": w.Q,
+            "a_mode": w.a_mode, "io_dtype": w.dtype, "global_batch": w.b * world, "seq_len": w.T,
+            "parallelism": "replicas x%d" % world}
+
+
+def roofline(w, kern_ms, peaks):
+    """Roofline of one launch: the slower of the algorithmic bytes at the HBM peak and the
+    algorithmic FLOPs at the bf16 tensor peak; frac = that time / the measured kernel time."""
+    from ssd_sequence_mixing_fwd_b300.inputs import algorithmic_bytes, algorithmic_flops
+    by = algorithmic_bytes(w)
+    fl = algorithmic_flops(w)
+    t_hbm = by / (peaks["hbm_gbs"] * 1e9)
+    t_tc = fl / (peaks["bf16_tflops"] * 1e12)
+    sec = kern_ms / 1e3
+    bound = "hbm" if t_hbm >= t_tc else "tensor"
+    achieved = by / sec / 1e9 if bound == "hbm" else fl / sec / 1e12
+    peak = peaks["hbm_gbs"] if bound == "hbm" else peaks["bf16_tflops"]
+    return {"bound": bound, "achieved": achieved, "peak": peak, "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
+            "frac": max(t_hbm, t_tc) / sec, "kernel_ms": kern_ms, "algorithmic_bytes": by,
+            "algorithmic_flops": fl, "t_hbm_us": t_hbm * 1e6, "t_tensor_us": t_tc * 1e6,
+            "peak_note": "%s of %s peaks (burst)" % ("hbm_gbs" if bound == "hbm" else "bf16_tflops", peaks["source"]),
+            "tensor_tflops": fl / sec / 1e12, "tensor_frac": fl / sec / 1e12 / peaks["bf16_tflops"]}
+
+
+def time_kernel(ssd, torch, w, dev, path, steps, warmup, flush):
+    """Kernel time (ms, mean over `steps`, L2 flushed before each) of one workload's dominant kernel."""
+    from ssd_sequence_mixing_fwd_b300.inputs import make_inputs
+    host = make_inputs(w)
+    d = {k: (None if v is None else v.to(dev)) for k, v in host.items()}
+    run = ssd.PreparedCall(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["init_state"], chunk_Q=w.Q,
+                           path=path)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(warmup):
+        flush.fill_(1.0)
+        run()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
+        flush.fill_(1.0)
+        ssd.ssd_debug_set_kernel_events(ev[i][0], ev[i][1])
+        run()
+    ssd.ssd_debug_set_kernel_events(None, None)
+    torch.cuda.synchronize(dev)
+    st = ssd.ssd_check_device_status(run.workspace, stream)
+    if st != 0:
+        raise ssd.SSDError(st, "secondary workload %s" % w.name)
+    ms = sum(e[0].elapsed_time(e[1]) for e in ev) / steps
+    return ms, ssd.ssd_fwd_path(run.dims), host
+
+
 # ---------------------------------------------------------------- CPU baseline
 def oracle_sample(w, inp, budget_s, nthreads=None):
     """Time the fp64 oracle on a bounded sample of workload ``w``.
@@ -321,23 +372,16 @@ def run_ours(args, w):
     peaks = load_peaks()
     by = algorithmic_bytes(w)
     fl = algorithmic_flops(w)
-    achieved = by / (kern_ms / 1e3) / 1e9
     out = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms_max,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f16-mma/f32" if path == "tcgen05" else "f32", "data": "synthetic",
-        "config": {"workload": w.name, "b": w.b, "T": w.T, "H": w.H, "P": w.P, "N": w.N, "G": w.G,
-                   "Q": w.Q, "a_mode": w.a_mode, "io_dtype": w.dtype, "path": path,
-                   "global_batch": w.b * world, "seq_len": w.T, "parallelism": "replicas x%d" % world,
-                   "l2": "flushed (256 MB write) before every timed step"},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / peaks["hbm_gbs"], "traffic": recorded_traffic(w, path),
-                     "kernel_ms": kern_ms, "algorithmic_bytes": by,
-                     "peak_note": "hbm_gbs of %s peaks (burst copy)" % peaks["source"],
-                     "tensor_tflops": fl / (kern_ms / 1e3) / 1e12,
-                     "tensor_frac": fl / (kern_ms / 1e3) / 1e12 / peaks["bf16_tflops"],
-                     "step_frac": (by / peaks["hbm_gbs"] / 1e9) / (step_ms_max / 1e3)},
+        "config": workload_config(w, world),
+        "path": path,
+        "l2": "flushed (256 MB write) before every timed step",
+        "roofline": dict(roofline(w, kern_ms, peaks), traffic=recorded_traffic(w, path),
+                         step_frac=(by / peaks["hbm_gbs"] / 1e9) / (step_ms_max / 1e3)),
         "e2e": {"value": tokens * world / (e2e_ms / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "pipeline": "two device buffer sets; step i's read-back overlaps step i+1's upload"},
@@ -347,6 +391,28 @@ def run_ours(args, w):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = oracle_sample(w, host, args.cpu_budget)
+    if rank == 0 and world == 1 and not args.no_secondary:
+        # the other workloads the parity targets are quoted on, timed in the same run: kernel time,
+        # roofline fraction, path, and the oracle on a bounded sample of each
+        from ssd_sequence_mixing_fwd_b300.inputs import WORKLOAD_ORDER, WORKLOADS
+        sec = {}
+        with ClockSampler(gpu_id) as clk2:
+            timed = {}
+            for name in WORKLOAD_ORDER:
+                if name == w.name:
+                    continue
+                w2 = WORKLOADS[name]
+                ms, p2, host2 = time_kernel(ssd, torch, w2, dev, args.path, 10, 3, flush)
+                timed[name] = (w2, ms, p2, host2)
+        for name, (w2, ms, p2, host2) in timed.items():
+            ent = {"path": p2, "kernel_ms": ms, "tokens_per_s": w2.tokens / (ms / 1e3),
+                   "roofline": roofline(w2, ms, peaks)}
+            if not args.no_cpu_baseline:
+                ent["cpu_baseline"] = oracle_sample(w2, host2, args.cpu_budget / 4)
+            sec[name] = ent
+        out["secondary"] = {"workloads": sec, "clocks": clk2.summary(),
+                            "timing": "10 launches after 3 warm-ups, L2 flushed before each, CUDA events "
+                                      "around the dominant kernel"}
     if dist is not None:
         dist.destroy_process_group()
     return out if rank == 0 else None
@@ -380,8 +446,7 @@ def run_reference(args, w):
             "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
-            "config": {"workload": w.name, "b": w.b, "T": w.T, "H": w.H, "P": w.P, "N": w.N,
-                       "G": w.G, "Q": w.Q, "a_mode": w.a_mode, "io_dtype": w.dtype},
+            "config": workload_config(w, world),
             "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                              "sample": "per step %d of %d (batch, head) streams over the full T=%d"
                                        % (n, total, w.T)},
@@ -399,6 +464,8 @@ def main(argv=None):
     ap.add_argument("--path", default="auto", choices=["auto", "generic", "tcgen05"],
                     help="kernel path (auto: the fused tcgen05 kernel where it applies)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip timing the other workloads (the `secondary` key)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch size (small cases for profiler captures)")

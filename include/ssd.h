@@ -30,7 +30,10 @@
  *     default stream).  The library never synchronises except in
  *     ssd_check_device_status.
  *   - Every function returns an int status (SSD_OK = 0).  All argument checks
- *     run before anything is enqueued; on any error nothing is enqueued.
+ *     run before anything is enqueued; on any argument error nothing is
+ *     enqueued (dims beyond a path's launch or index limits are rejected as
+ *     SSD_ERR_UNSUPPORTED there).  A CUDA runtime failure while enqueueing
+ *     returns SSD_ERR_CUDA and may leave the work enqueued before it.
  *   - Not reentrant on one workspace: two calls that share a workspace must be
  *     ordered on the GPU (same stream or an event between them).
  */
@@ -82,9 +85,12 @@ extern "C" {
  *   Q in {64, 128, 256}.
  * b == 0 or T == 0 is a valid empty problem: y is empty and final_state is
  * init_state (or zero).  A ragged last chunk (T % Q != 0) is allowed.
- * Domain (not checked on the device): dt >= 0 and A <= 0, all finite; the
- * fused path keeps matrix operands in fp16, so |x|, |B|, |C| and the state
- * entries must stay below 65504. */
+ * Domain (not checked on the device): dt >= 0 and A <= 0, all finite.  The
+ * fused path keeps its matrix operands in fp16: when x, B, C, a C B^T entry
+ * or a state entry entering a 128-token block leaves the fp16 range
+ * (|v| > 65504), the call reports SSD_ERR_DEVICE through
+ * ssd_check_device_status and its outputs are invalid; the generic path has
+ * no such limit (SSD_PATH_GENERIC computes such inputs in fp32). */
 typedef struct ssd_dims {
     int64_t b, T, H, P, N, G, Q;
     int32_t a_mode;    /* SSD_A_SCALAR or SSD_A_DIAGONAL                       */
@@ -166,13 +172,17 @@ SSD_API int ssd_debug_set_wait(int64_t spin_limit, int64_t withhold_chunk);
  * generic path with its scratch in one fixed array of
  * SSD_NOALLOC_SCRATCH_BYTES (64 MiB) compiled into the library.  Every GPU
  * that loads the library holds that array until the process exits.  A
- * problem whose scratch (256 B + 4*b*H*nc + 4*b*H*nc*N*P bytes, nc =
- * ceil(T/Q)) does not fit is rejected with SSD_ERR_SCRATCH_LIMIT before
- * anything is enqueued.  The function calls no cudaMalloc, cudaFree or other
- * allocating routine.
+ * problem whose scratch (256 + align256(4*b*H*nc) + 4*b*H*nc*N*P bytes,
+ * nc = ceil(T/Q), align256 rounding up to a multiple of 256) does not fit
+ * is rejected with SSD_ERR_SCRATCH_LIMIT before anything is enqueued.  The
+ * function calls no cudaMalloc, cudaFree or other allocating routine.
  *
  * The first call on each device looks up that device's address of the array
  * (with the device current); make that first call before any stream capture.
+ * The address is cached with the context it belongs to and looked up again
+ * when the current context differs (for example after cudaDeviceReset); a
+ * call right after such a change does that lookup, so it too should come
+ * before any stream capture.
  * All calls in the process share the one array and it keeps the previous
  * call's contents (the status word is cleared by each call), so calls whose
  * executions overlap on the GPU -- on different streams, or from different

@@ -211,7 +211,14 @@ def ssd_fwd(x, dt, A, B, C, D=None, init_state=None, chunk_Q=256, return_final_s
 
     ``y``, ``final_state`` and ``workspace`` may be passed preallocated
     (workspace: uint8 CUDA tensor of at least ``ssd_fwd_workspace_size``
-    bytes).  ``check=True`` synchronises and raises on a device-side error.
+    bytes).
+
+    The call is asynchronous.  Errors the kernels find on the device -- a
+    bounded wait between blocks that ran out (SSD_ERR_TIMEOUT; the kernel then
+    continues with a zero state) or an operand outside the fused path's fp16
+    range (SSD_ERR_DEVICE) -- leave y and final_state invalid WITHOUT raising,
+    unless ``check=True`` (which synchronises and raises) or the caller reads
+    the status with ``ssd_check_device_status(workspace)`` afterwards.
     """
     dims, args, y, final_state, workspace, s = _marshal(
         x, dt, A, B, C, D, init_state, chunk_Q, return_final_state, path, y, final_state, workspace, stream)

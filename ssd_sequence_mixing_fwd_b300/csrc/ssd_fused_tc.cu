@@ -121,8 +121,10 @@ __device__ __forceinline__ void decode_item(const FusedParams &p, int t, int &bi
 
 // C and B of a stage, bf16 -> fp16 in place: row r of each of the nbox boxes.  Chunk
 // c ^ (r & 7): eight consecutive rows touch eight different 16-byte bank groups (walking
-// chunk c of every row would put a quarter warp on the same four banks).
-__device__ __noinline__ void convert_stage_rows(unsigned char *base, int nbox, int r) {
+// chunk c of every row would put a quarter warp on the same four banks).  Returns nonzero
+// when a value left the fp16 range.
+__device__ __noinline__ uint32_t convert_stage_rows(unsigned char *base, int nbox, int r) {
+    uint32_t bad = 0;
     const uint32_t rx = (uint32_t)(r & 7) * 16u;
 #pragma unroll 1
     for (int bx = 0; bx < nbox; ++bx) {
@@ -136,9 +138,11 @@ __device__ __noinline__ void convert_stage_rows(unsigned char *base, int nbox, i
             u[c].y = bf2_to_h2(u[c].y);
             u[c].z = bf2_to_h2(u[c].z);
             u[c].w = bf2_to_h2(u[c].w);
+            bad |= h8_nonfinite(u[c]);
             *reinterpret_cast<uint4 *>(row + ((16u * c) ^ rx)) = u[c];
         }
     }
+    return bad;
 }
 
 template <int NS>
@@ -434,6 +438,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_off = (uint32_t)(32 * q) << 16;
         const bool leader = (warp == 2 + 4 * g) && lane == 0;
         float *vq = vS + 512 * g;
+        // nonzero once a matrix operand of this thread left the fp16 range (C, B, x, h_prev; and
+        // C B^T, which bounds S since every decay factor is <= 1): reported at the end
+        uint32_t bad = 0;
         unsigned char *xbuf = smem + kOffGroup + g * kGroupBytes;
         unsigned char *wbuf = xbuf + kBox;
         {
@@ -466,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // (N = 128: a warp that found this stage already landed during its last head of the
             // previous item has converted its rows then, while it waited for C h_prev)
             if (j0 == 0 && !conv_ahead) {
-                convert_stage_rows(smem + kOffStage + st * kStage, 4 * NS, r);
+                bad |= convert_stage_rows(smem + kOffStage + st * kStage, 4 * NS, r);
                 if (!p.dt_tma) {
                     // dt tile by thread loads (rows past the sequence end are zero)
                     float *tile = dtT + st * (kBlk * kMaxK);
@@ -532,6 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int e = 0; e < 4; ++e) {
                                 const float2 f = bf2_to_f2(uw[e]);
                                 xo[e] = pack_h2f(f);
+                                bad |= h2_nonfinite(xo[e]);
                                 wo[e] = pack_h2f(mul2(f, w2));
                                 const float2 dv = mul2(f, d2);
                                 dx[8 * cc + 2 * e] = dv.x;
@@ -565,6 +573,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         float c[32];
                         tmem_ld32(tmem + lane_off + kTmCB + 32 * J, c);
                         tmem_ld_wait();
+                        if (s == 0) {
+                            // once per item: C B^T within the fp16 range
+                            float cm = 0.f;
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) cm = fmaxf(cm, fabsf(c[e]));
+                            bad |= (cm > kF16Max) ? 1u : 0u;
+                        }
                         if (J < q) {
                             const float2 *vv = reinterpret_cast<const float2 *>(vq + 128 * q + 32 * J);
 #pragma unroll
@@ -654,8 +669,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int cc = 0; cc < 8; ++cc) {
                             const float4 u0 = hp[2 * cc], u1 = hp[2 * cc + 1];
-                            *reinterpret_cast<uint4 *>(hpbuf + swz(nrow, cc)) =
+                            const uint4 hv =
                                 make_uint4(pack_h2(u0.x, u0.y), pack_h2(u0.z, u0.w), pack_h2(u1.x, u1.y), pack_h2(u1.z, u1.w));
+                            bad |= h8_nonfinite(hv);
+                            *reinterpret_cast<uint4 *>(hpbuf + swz(nrow, cc)) = hv;
                         }
                         fence_async_smem();
                         tc_fence_before();
@@ -686,9 +703,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     if constexpr (NS == 2) {
 #pragma unroll
-                        for (int cc = 0; cc < 8; ++cc)
-                            *reinterpret_cast<uint4 *>(hpbuf + swz(nrow, cc)) =
-                                make_uint4(hk[4 * cc], hk[4 * cc + 1], hk[4 * cc + 2], hk[4 * cc + 3]);
+                        for (int cc = 0; cc < 8; ++cc) {
+                            const uint4 hv = make_uint4(hk[4 * cc], hk[4 * cc + 1], hk[4 * cc + 2], hk[4 * cc + 3]);
+                            bad |= h8_nonfinite(hv);
+                            *reinterpret_cast<uint4 *>(hpbuf + swz(nrow, cc)) = hv;
+                        }
                         // N = 256 (chain-bound): each warp publishes its own 32 rows of each half
                         // as soon as they are stored -- every lane fences its stores at GPU
                         // scope, then one lane bumps the quarter's counter -- so the next block's
@@ -735,7 +754,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const bool landed = __shfl_sync(0xffffffffu,
                                                         lane == 0 ? (int)mbar_test(bar(B_CB_FULL + st2), ((it + 1) / NST) & 1) : 0, 0);
                         if (landed && itemS[st2] >= 0) {
-                            convert_stage_rows(smem + kOffStage + st2 * kStage, 4 * NS, r);
+                            bad |= convert_stage_rows(smem + kOffStage + st2 * kStage, 4 * NS, r);
                             fence_async_smem();
                             __syncwarp();
                             if (lane == 0) mbar_arrive(bar(B_CB_CONV + st2));
@@ -805,6 +824,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             pubS[2 * g] = -1;
             mbar_arrive_cnt(bar(B_PUB_FULL + g), 4);
         }
+        if (__any_sync(0xffffffffu, bad != 0) && lane == 0) set_status(p.status, SSD_ERR_DEVICE);
     }
 
     tc_fence_before();
@@ -859,8 +879,9 @@ bool fused_supports(const Problem &p) {
     if (p.P != kP || (p.N != 128 && p.N != 256)) return false;
     if (p.Q != 128 && p.Q != 256) return false;
     if (p.T > (int64_t)INT32_MAX / 2 || p.b * p.H * 2 > (int64_t)INT32_MAX) return false;
-    const int64_t items = ((p.T + kBlk - 1) / kBlk) * p.b * (p.H / heads_per_item(p));
-    return items < (int64_t)INT32_MAX;
+    // the kernel indexes items and flat head numbers (items x heads per item) in 32 bits
+    const int64_t blocks = (p.T + kBlk - 1) / kBlk;
+    return blocks * p.b * p.H < (int64_t)INT32_MAX;
 }
 
 size_t fused_workspace_bytes(const Problem &p) {

@@ -447,6 +447,9 @@ cudaError_t launch_typed(const Problem &p, const GenericWorkspace &w, cudaStream
 
 bool generic_supports(const Problem &p) {
     if (p.P < 1 || p.P > 256 || (p.P & (p.P - 1))) return false;
+    // launch limits of the three grids: (chunks [x 32-row tiles], H, b)
+    if (p.H > 65535 || p.b > 65535) return false;
+    if (p.nc * ((p.Q + kRT - 1) / kRT) > (int64_t)INT32_MAX) return false;
     if (p.N < 1 || p.N > 256 || p.N * p.P > (int64_t)kMaxAcc * kThreads) return false;
     if (p.Q > kThreads) return false;
     if (kRT * p.P > (int64_t)kMaxOut * kThreads) return false;

@@ -10,6 +10,8 @@
 // keeps until the process exits.  All calls share it, so calls that overlap on
 // the GPU race; it keeps the previous call's contents, and the only part that
 // must start at zero (the status word) is cleared by every call.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "ssd_internal.cuh"
@@ -21,20 +23,50 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[SSD_NOALLOC_SCR
 
 constexpr int kMaxDevices = 128;
 std::mutex g_scratch_mu;
+// Per device: the array's device address and the unique ID of the context it was looked up in.
 void *g_scratch_addr[kMaxDevices] = {};
+unsigned long long g_scratch_ctx[kMaxDevices] = {};
 
-// Device address of g_noalloc_scratch on the current device.  In host code the
-// array's name is only a host-side stand-in, so the address is looked up once
-// per device, with that device current, and cached.
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+
+template <typename Fn>
+Fn driver_fn(const char *name) {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return reinterpret_cast<Fn>(f);
+}
+
+// Unique ID of the calling thread's current context (0 when there is none or it cannot be read).
+unsigned long long current_ctx_id() {
+    static CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+    static CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+    if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+// Device address of g_noalloc_scratch on the current device.  In host code the array's name is
+// only a host-side stand-in, so the address is looked up with the device current.  It is cached
+// together with the context it belongs to and looked up again when the current context differs
+// (after cudaDeviceReset, or after the primary context was released and created anew, the
+// module is loaded again and the array can move).
 int scratch_on_current_device(void **out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SSD_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
+    const unsigned long long ctx = current_ctx_id();
+    if (!g_scratch_addr[dev] || ctx == 0 || ctx != g_scratch_ctx[dev]) {
         void *p = nullptr;
         const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess || p == nullptr) return SSD_ERR_CUDA;
         g_scratch_addr[dev] = p;
+        g_scratch_ctx[dev] = current_ctx_id();   // the lookup makes the primary context current
     }
     *out = g_scratch_addr[dev];
     return SSD_OK;

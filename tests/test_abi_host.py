@@ -116,3 +116,30 @@ def test_null_and_misaligned_pointers_rejected_before_any_launch(lib):
 def test_path_query(lib):
     assert ssd.ssd_fwd_path(dims(path="generic")) == "generic"
     assert ssd.ssd_fwd_path(dims(dtype="f32")) in ("generic", "tcgen05")
+
+
+@pytest.mark.parametrize("big", [dict(H=70000, G=70000), dict(b=70000)], ids=["H_over_grid_y", "b_over_grid_z"])
+def test_dims_beyond_launch_limits_rejected_before_enqueue(lib, big):
+    # The generic path's grids put H and b on grid dimensions y and z (at most 65535 each):
+    # such dims are refused at validation, before anything is enqueued.
+    for a_mode in ("scalar", "diagonal"):
+        d = dims(path="generic", a_mode=a_mode, **big)
+        with pytest.raises(ssd.SSDError) as e:
+            ssd.ssd_fwd_workspace_size(d)
+        assert e.value.status == ssd.SSD_ERR_UNSUPPORTED
+    # diagonal A has no fused path, so AUTO has nothing to fall back to either
+    with pytest.raises(ssd.SSDError) as e:
+        ssd.ssd_fwd_workspace_size(dims(a_mode="diagonal", **big))
+    assert e.value.status == ssd.SSD_ERR_UNSUPPORTED
+    # and ssd_fwd itself returns the same status without touching the (fake) device pointers
+    d = dims(path="generic", **big)
+    args = [ctypes.c_void_p((1 << 21) + 4096 * i) for i in range(9)]
+    assert lib.ssd_fwd(ctypes.byref(d), *args, ctypes.c_void_p(1 << 20), 1 << 40, None) == ssd.SSD_ERR_UNSUPPORTED
+
+
+def test_fused_path_index_limit(lib):
+    # blocks x b x H must stay below 2^31 on the fused path (32-bit item and head numbers)
+    d = dims(b=64, T=1 << 24, H=4096, G=4096, path="tcgen05")
+    with pytest.raises(ssd.SSDError) as e:
+        ssd.ssd_fwd_workspace_size(d)
+    assert e.value.status == ssd.SSD_ERR_UNSUPPORTED

@@ -5,9 +5,9 @@ themselves (for example a plug-in whose host application owns the whole
 device-memory budget, or a latency-bound loop where cudaMalloc's possible
 device synchronisation is not allowed).  It uses a fixed scratch array inside
 the library instead of a caller workspace.  These tests compare it with the
-ordinary entry point ssd_fwd on two calls in a row with different inputs (the
-array keeps the previous call's contents, so the second call must not depend
-on them), and check that a problem too large for the array is refused before
+ordinary entry point ssd_fwd on three calls in a row, the last two of the
+same shape with different inputs (the array keeps the previous call's
+contents, so a call must not depend on them), and check that a problem too large for the array is refused before
 any GPU work.  The file sorts last so that a stop-at-first-failure run has
 already run every other test when it gets here.
 """
@@ -53,13 +53,17 @@ def test_noalloc_rejects_problem_larger_than_its_scratch():
 
 
 @pytest.mark.gpu
-def test_noalloc_matches_ssd_fwd_on_two_calls_in_a_row(cuda_device):
+def test_noalloc_matches_ssd_fwd_on_calls_in_a_row(cuda_device):
     lib = ssd.load_library()
     stream = torch.cuda.current_stream(cuda_device)
+    # the second and third calls have the same shape with different inputs: the array still
+    # holds the second call's chunk states when the third one starts
     cases = [
         Workload("na1", b=2, T=1000, H=4, P=64, N=128, G=2, Q=128, D="normal", init_std=0.1, seed=901),
         Workload("na2", b=1, T=777, H=6, P=64, N=64, G=3, Q=256, a_mode="diagonal", D="none",
                  init_std=0.2, seed=902),
+        Workload("na3", b=1, T=777, H=6, P=64, N=64, G=3, Q=256, a_mode="diagonal", D="none",
+                 init_std=0.2, seed=903),
     ]
     for w in cases:
         d = {k: (None if v is None else v.to(cuda_device)) for k, v in make_inputs(w).items()}
