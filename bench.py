@@ -197,6 +197,10 @@ def time_kernel(ssd, torch, w, dev, path, steps, warmup, flush):
         flush.fill_(1.0)
         run()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for e in ev:                      # torch creates an event's handle on its first record
+        for x in e:
+            x.record(stream)
+    torch.cuda.synchronize(dev)
     for i in range(steps):
         flush.fill_(1.0)
         ssd.ssd_debug_set_kernel_events(ev[i][0], ev[i][1])

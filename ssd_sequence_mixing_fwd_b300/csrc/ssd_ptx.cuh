@@ -216,17 +216,11 @@ __device__ __forceinline__ uint32_t bf2_to_h2(uint32_t u) {
     float2 f = __bfloat1622float2(b);
     return pack_h2(f.x, f.y);
 }
-// Nonzero when either fp16 half of `u` is infinite or NaN (exponent field all ones): adding one to
-// a saturated 5-bit exponent carries into the sign bit.
-__device__ __forceinline__ uint32_t h2_nonfinite(uint32_t u) {
-    return ((u & 0x7C007C00u) + 0x04000400u) & 0x80008000u;
+// Nonzero when either bf16 half of `u` is infinite or NaN (exponent field all ones): adding one to
+// a saturated 8-bit exponent carries into the sign bit.
+__device__ __forceinline__ uint32_t bf2_nonfinite(uint32_t u) {
+    return ((u & 0x7F807F80u) + 0x00800080u) & 0x80008000u;
 }
-__device__ __forceinline__ uint32_t h8_nonfinite(uint4 u) {
-    return h2_nonfinite(u.x) | h2_nonfinite(u.y) | h2_nonfinite(u.z) | h2_nonfinite(u.w);
-}
-// Largest finite fp16 value: matrix operands of the fused kernels are fp16, so a value beyond it
-// (after the kernels' rounding) is reported as SSD_ERR_DEVICE instead of being used as inf.
-constexpr float kF16Max = 65504.f;
 
 // Byte offset of 16-byte chunk c of row r in a 128-byte-row, 128B-swizzled tile.
 __device__ __forceinline__ uint32_t swz(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
