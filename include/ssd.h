@@ -25,7 +25,8 @@
  *   - All tensor arguments are DEVICE pointers to dense row-major arrays in
  *     the layouts given below, owned by the caller.  The library allocates no
  *     memory and keeps no pointer after a call returns.
- *   - Every pointer must be 16-byte aligned (SSD_ERR_ALIGNMENT otherwise).
+ *   - Every pointer must be 16-byte aligned (SSD_ERR_ALIGNMENT otherwise),
+ *     except in ssd_scan and ssd_decode_step (element alignment).
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
  *     default stream).  The library never synchronises except in
  *     ssd_check_device_status.
@@ -161,6 +162,40 @@ SSD_API int ssd_abi_version(void);
  * ssd_check_device_status.  Process-wide; not for production use.
  * Returns SSD_OK. */
 SSD_API int ssd_debug_set_wait(int64_t spin_limit, int64_t withhold_chunk);
+
+/* Linear form.  The same map as ssd_fwd, same arguments and layouts, no
+ * workspace, evaluated by the recurrence itself, token by token, on CUDA
+ * cores: one block per (batch row, head) keeps the N x P state in registers
+ * for the whole sequence (Structured State Space Duality, "The recurrence as
+ * one matrix": the O(T) linear form, against which the pages set the
+ * chunked algorithm).  dims->path must be SSD_PATH_AUTO; dims->Q is checked
+ * like ssd_fwd's but not used.  Supported: every dims ssd_fwd accepts.
+ * init_state and final_state may be the same buffer (the state is then
+ * updated in place).  Pointers need only element alignment here (2 bytes
+ * for bf16, 4 for float32), not the 16 bytes of ssd_fwd.  Arithmetic in fp32; the result equals ssd_fwd's up to
+ * rounding ("When it breaks": the forms are not bit-identical).  Returns
+ * after enqueueing one kernel; the linear form has no device-side waits, so
+ * the return value is the whole status. */
+SSD_API int ssd_scan(const ssd_dims *dims,
+            const void *x, const float *dt, const float *A,
+            const void *B, const void *C, const float *D,
+            const float *init_state,
+            void *y, float *final_state,
+            void *stream);
+
+/* One decode step: ssd_scan with dims->T == 1 and the state updated in place.
+ *   x (b,1,H,P), dt (b,1,H), B and C (b,1,G,N) for the new token; A and D as
+ *   in ssd_fwd; state (b,H,N,P) float32, read and overwritten with
+ *   h_t = a_t (.) h_{t-1} + B_t x_t^T; y (b,1,H,P) written with
+ *   C_t^T h_t + D x_t.
+ * A model that ran ssd_fwd over a prompt continues from its final_state with
+ * one call per generated token.  SSD_ERR_INVALID_ARG unless dims->T == 1
+ * and state is non-NULL. */
+SSD_API int ssd_decode_step(const ssd_dims *dims,
+            const void *x, const float *dt, const float *A,
+            const void *B, const void *C, const float *D,
+            float *state, void *y,
+            void *stream);
 
 /* Allocation-free forward pass.  The paper has no counterpart to this entry
  * point; it exists for callers that may not allocate device memory

@@ -42,7 +42,8 @@ _PATHS = {"auto": SSD_PATH_AUTO, "generic": SSD_PATH_GENERIC, "tcgen05": SSD_PAT
 # Every symbol include/ssd.h declares.
 EXPORTED = ("ssd_fwd_workspace_size", "ssd_fwd_path", "ssd_fwd", "ssd_check_device_status",
             "ssd_status_string", "ssd_abi_version", "ssd_debug_set_wait",
-            "ssd_debug_set_kernel_events", "ssd_launch_count", "ssd_fwd_noalloc", "ssd_last_cuda_error")
+            "ssd_debug_set_kernel_events", "ssd_launch_count", "ssd_fwd_noalloc", "ssd_last_cuda_error",
+            "ssd_scan", "ssd_decode_step")
 
 
 class ssd_dims(ctypes.Structure):
@@ -79,6 +80,8 @@ def load_library(path=LIB_PATH):
             lib.ssd_fwd_path.argtypes = [P_dims, ctypes.POINTER(ctypes.c_int32)]
             lib.ssd_fwd.argtypes = [P_dims] + [vp] * 9 + [vp, sz, vp]
             lib.ssd_fwd_noalloc.argtypes = [P_dims] + [vp] * 9 + [vp]
+            lib.ssd_scan.argtypes = [P_dims] + [vp] * 9 + [vp]
+            lib.ssd_decode_step.argtypes = [P_dims] + [vp] * 8 + [vp]
             lib.ssd_check_device_status.argtypes = [vp, sz, vp]
             lib.ssd_status_string.argtypes = [ctypes.c_int]
             lib.ssd_status_string.restype = ctypes.c_char_p
@@ -90,7 +93,8 @@ def load_library(path=LIB_PATH):
             lib.ssd_launch_count.argtypes = [ctypes.POINTER(ctypes.c_uint64)]
             for name in ("ssd_fwd_workspace_size", "ssd_fwd_path", "ssd_fwd",
                          "ssd_check_device_status", "ssd_abi_version", "ssd_debug_set_wait",
-                         "ssd_debug_set_kernel_events", "ssd_launch_count", "ssd_fwd_noalloc"):
+                         "ssd_debug_set_kernel_events", "ssd_launch_count", "ssd_fwd_noalloc",
+                         "ssd_scan", "ssd_decode_step"):
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -163,6 +167,9 @@ def ssd_launch_count():
     return n.value
 
 
+_NO_WORKSPACE = object()     # marshal without a workspace (entry points that take none)
+
+
 def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
@@ -197,11 +204,14 @@ def _marshal(x, dt, A, B, C, D, init_state, chunk_Q, return_final_state, path, y
         y = torch.empty_like(x)
     if final_state is None and return_final_state:
         final_state = torch.empty((b, H, N, P), device=dev, dtype=torch.float32)
-    if workspace is None:
+    if workspace is _NO_WORKSPACE:
+        workspace = None
+    elif workspace is None:
         workspace = torch.empty(max(ssd_fwd_workspace_size(dims), 256), device=dev, dtype=torch.uint8)
     s = torch.cuda.current_stream(dev) if stream is None else stream
     args = (ctypes.byref(dims), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(init_state),
-            _ptr(y), _ptr(final_state), _ptr(workspace), workspace.numel(), ctypes.c_void_p(s.cuda_stream))
+            _ptr(y), _ptr(final_state), _ptr(workspace), 0 if workspace is None else workspace.numel(),
+            ctypes.c_void_p(s.cuda_stream))
     return dims, args, y, final_state, workspace, s
 
 
@@ -230,6 +240,34 @@ def ssd_fwd(x, dt, A, B, C, D=None, init_state=None, chunk_Q=256, return_final_s
         if st != SSD_OK:
             raise SSDError(st, "ssd_fwd (device)")
     return y, final_state
+
+
+def ssd_scan(x, dt, A, B, C, D=None, init_state=None, return_final_state=True, y=None, final_state=None,
+             stream=None):
+    """The same map as :func:`ssd_fwd`, evaluated by the linear recurrence token by token on CUDA
+    cores (no workspace).  Returns ``(y, final_state)``."""
+    dims, args, y, final_state, _, s = _marshal(
+        x, dt, A, B, C, D, init_state, 256, return_final_state, "auto", y, final_state, _NO_WORKSPACE, stream)
+    st = load_library().ssd_scan(*(args[:10] + args[12:]))
+    if st != SSD_OK:
+        raise SSDError(st, "ssd_scan")
+    return y, final_state
+
+
+def ssd_decode_step(x, dt, A, B, C, D, state, y=None, stream=None):
+    """One generated token: x (b,1,H,P), dt (b,1,H), B and C (b,1,G,N); ``state`` (b,H,N,P) fp32 is
+    updated in place.  Returns y (b,1,H,P)."""
+    import torch
+    if state is None or state.dtype != torch.float32 or not state.is_cuda or not state.is_contiguous():
+        raise ValueError("state must be a contiguous float32 CUDA tensor")
+    if x.shape[1] != 1:
+        raise ValueError("a decode step takes one token (x of shape (b,1,H,P))")
+    dims, args, y, _, _, s = _marshal(
+        x, dt, A, B, C, D, state, 256, False, "auto", y, None, _NO_WORKSPACE, stream)
+    st = load_library().ssd_decode_step(args[0], *args[1:7], _ptr(state), args[8], args[12])
+    if st != SSD_OK:
+        raise SSDError(st, "ssd_decode_step")
+    return y
 
 
 class PreparedCall:

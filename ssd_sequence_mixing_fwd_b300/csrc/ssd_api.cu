@@ -172,6 +172,53 @@ extern "C" int ssd_fwd(const ssd_dims *dims, const void *x, const float *dt, con
     return note_cuda(e);
 }
 
+// The linear form (ssd_scan) and its one-token case (ssd_decode_step): same argument checks as
+// ssd_fwd, no workspace.
+static int scan_call(const ssd_dims *dims, const void *x, const float *dt, const float *A, const void *B,
+                     const void *C, const float *D, const float *init_state, void *y, float *final_state,
+                     void *stream) {
+    Problem p;
+    int st = check_dims(dims, &p);
+    if (st != SSD_OK) return st;
+    if (dims->path != SSD_PATH_AUTO) return SSD_ERR_INVALID_ARG;
+    if (!scan_supports(p)) return SSD_ERR_UNSUPPORTED;
+    const bool empty = (p.b == 0 || p.T == 0);
+    if (!empty && (!x || !dt || !A || !B || !C || !y)) return SSD_ERR_INVALID_ARG;
+    // element alignment only (the linear form reads elements one by one): a decode step's
+    // token is usually a slice of a larger buffer
+    const uintptr_t io_mask = p.io_dtype == SSD_DTYPE_BF16 ? 1u : 3u;
+    const void *io_ptrs[] = {x, B, C, y};
+    for (const void *q : io_ptrs)
+        if (q && (reinterpret_cast<uintptr_t>(q) & io_mask)) return SSD_ERR_ALIGNMENT;
+    const void *f32_ptrs[] = {dt, A, D, init_state, final_state};
+    for (const void *q : f32_ptrs)
+        if (q && (reinterpret_cast<uintptr_t>(q) & 3u)) return SSD_ERR_ALIGNMENT;
+    if (!empty && y == x) return SSD_ERR_INVALID_ARG;
+    p.x = x; p.dt = dt; p.A = A; p.B = B; p.C = C; p.D = D;
+    p.init = init_state; p.y = y; p.final_state = final_state;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (empty) {
+        // final_state <- init_state (an in-place state is already there)
+        if (!final_state || final_state == init_state) return SSD_OK;
+        return note_cuda(launch_copy_state(p, s));
+    }
+    return note_cuda(scan_launch(p, s));
+}
+
+extern "C" int ssd_scan(const ssd_dims *dims, const void *x, const float *dt, const float *A, const void *B,
+                        const void *C, const float *D, const float *init_state, void *y, float *final_state,
+                        void *stream) {
+    return scan_call(dims, x, dt, A, B, C, D, init_state, y, final_state, stream);
+}
+
+extern "C" int ssd_decode_step(const ssd_dims *dims, const void *x, const float *dt, const float *A,
+                               const void *B, const void *C, const float *D, float *state, void *y,
+                               void *stream) {
+    if (!dims) return SSD_ERR_INVALID_ARG;
+    if (dims->T != 1 || !state) return SSD_ERR_INVALID_ARG;
+    return scan_call(dims, x, dt, A, B, C, D, state, y, state, stream);
+}
+
 extern "C" int ssd_check_device_status(void *workspace, size_t workspace_bytes, void *stream) {
     if (!workspace || workspace_bytes < sizeof(int)) return SSD_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

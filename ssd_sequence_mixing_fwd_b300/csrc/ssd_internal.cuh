@@ -51,6 +51,10 @@ size_t fused_workspace_bytes(const Problem &p);
 bool fused_supports(const Problem &p);
 cudaError_t fused_launch(const Problem &p, void *ws, size_t ws_bytes, cudaStream_t s);
 
+// ---- linear-form scan (csrc/ssd_scan.cu): no workspace ---------------------
+bool scan_supports(const Problem &p);
+cudaError_t scan_launch(const Problem &p, cudaStream_t s);
+
 // ---- small helpers (csrc/ssd_api.cu) --------------------------------------
 // Host-side validation of ssd_dims shared by the entry points (fills *prob).
 int validate_dims(const ssd_dims *d, Problem *prob);

@@ -143,3 +143,21 @@ def test_fused_path_index_limit(lib):
     with pytest.raises(ssd.SSDError) as e:
         ssd.ssd_fwd_workspace_size(d)
     assert e.value.status == ssd.SSD_ERR_UNSUPPORTED
+
+
+def test_scan_and_decode_reject_bad_arguments_before_any_launch(lib):
+    args = [ctypes.c_void_p((1 << 21) + 4096 * i) for i in range(9)]
+    # decode: exactly one token, and a state
+    d = dims(T=5)
+    assert lib.ssd_decode_step(ctypes.byref(d), *args[:6], args[6], args[7], None) == ssd.SSD_ERR_INVALID_ARG
+    d = dims(T=1)
+    assert lib.ssd_decode_step(ctypes.byref(d), *args[:6], None, args[7], None) == ssd.SSD_ERR_INVALID_ARG
+    # scan: no path selection, aligned pointers, invalid dims
+    assert lib.ssd_scan(ctypes.byref(dims(path="generic")), *args, None) == ssd.SSD_ERR_INVALID_ARG
+    a = list(args)
+    a[0] = ctypes.c_void_p((1 << 21) + 1)                # odd address for bf16 x
+    assert lib.ssd_scan(ctypes.byref(dims()), *a, None) == ssd.SSD_ERR_ALIGNMENT
+    a = list(args)
+    a[1] = ctypes.c_void_p((1 << 21) + 4096 + 2)         # dt not 4-byte aligned
+    assert lib.ssd_scan(ctypes.byref(dims()), *a, None) == ssd.SSD_ERR_ALIGNMENT
+    assert lib.ssd_scan(ctypes.byref(dims(Q=96)), *args, None) == ssd.SSD_ERR_INVALID_ARG
