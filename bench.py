@@ -396,6 +396,23 @@ def run_ours(args, w):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = oracle_sample(w, host, args.cpu_budget)
     if rank == 0 and world == 1 and not args.no_secondary:
+        # the linear form (ssd_scan: the recurrence token by token on CUDA cores) on the same
+        # inputs: the comparison the pages draw between the two forms (context, not a target)
+        lin = []
+        for i in range(4):
+            flush.fill_(1.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            ssd.ssd_scan(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["init_state"], stream=stream)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            if i >= 1:
+                lin.append(e0.elapsed_time(e1))
+        lin_ms = sum(lin) / len(lin)
+        out["linear_form"] = {"kernel_ms": lin_ms, "tokens_per_s": w.tokens / (lin_ms / 1e3),
+                              "chunked_speedup": lin_ms / kern_ms,
+                              "note": "ssd_scan on the same inputs, 3 launches after 1 warm-up; "
+                                      "chunked_speedup = linear-form time / chunked kernel time"}
         # the other workloads the parity targets are quoted on, timed in the same run: kernel time,
         # roofline fraction, path, and the oracle on a bounded sample of each
         from ssd_sequence_mixing_fwd_b300.inputs import WORKLOAD_ORDER, WORKLOADS
