@@ -43,7 +43,7 @@ int check_dims(const ssd_dims *d, Problem *prob) {
 
 // Which path runs for these dims (after check_dims succeeded).
 int choose_path(const ssd_dims *d, const Problem &p, int32_t *path) {
-    const bool tc = fused_supports(p);
+    const bool tc = fused_supports(p) || diag_supports(p);
     const bool gen = generic_supports(p);
     if (d->path == SSD_PATH_TCGEN05) {
         if (!tc) return SSD_ERR_UNSUPPORTED;
@@ -60,7 +60,8 @@ int choose_path(const ssd_dims *d, const Problem &p, int32_t *path) {
 }
 
 size_t workspace_for(const Problem &p, int32_t path) {
-    return path == SSD_PATH_TCGEN05 ? fused_workspace_bytes(p) : generic_workspace_bytes(p);
+    if (path == SSD_PATH_TCGEN05) return diag_supports(p) ? diag_workspace_bytes(p) : fused_workspace_bytes(p);
+    return generic_workspace_bytes(p);
 }
 
 __global__ void copy_state_kernel(const float *init, float *out, int64_t n) {
@@ -164,7 +165,8 @@ extern "C" int ssd_fwd(const ssd_dims *dims, const void *x, const float *dt, con
 
     cudaError_t e;
     if (!empty && path == SSD_PATH_TCGEN05) {
-        e = fused_launch(p, workspace, workspace_bytes, s);   // clears its own status block and counters
+        // each clears its own status block (and counters)
+        e = diag_supports(p) ? diag_launch(p, workspace, s) : fused_launch(p, workspace, workspace_bytes, s);
     } else {
         e = cudaMemsetAsync(workspace, 0, kStatusBytes, s);
         if (e == cudaSuccess) e = empty ? launch_copy_state(p, s) : generic_launch(p, generic_carve(p, workspace), s);

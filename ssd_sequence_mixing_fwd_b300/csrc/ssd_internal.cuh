@@ -51,6 +51,11 @@ size_t fused_workspace_bytes(const Problem &p);
 bool fused_supports(const Problem &p);
 cudaError_t fused_launch(const Problem &p, void *ws, size_t ws_bytes, cudaStream_t s);
 
+// ---- diagonal-A tcgen05 path (csrc/ssd_diag_tc.cu); workspace: the status block
+bool diag_supports(const Problem &p);
+size_t diag_workspace_bytes(const Problem &p);
+cudaError_t diag_launch(const Problem &p, void *ws, cudaStream_t s);
+
 // ---- linear-form scan (csrc/ssd_scan.cu): no workspace ---------------------
 bool scan_supports(const Problem &p);
 cudaError_t scan_launch(const Problem &p, cudaStream_t s);

@@ -118,6 +118,20 @@ def test_path_query(lib):
     assert ssd.ssd_fwd_path(dims(dtype="f32")) in ("generic", "tcgen05")
 
 
+def test_diagonal_path_selection(lib):
+    # diagonal A runs on tcgen05 for bf16 io with N = P = 64 (any Q, G, T); otherwise generic
+    assert ssd.ssd_fwd_path(dims(a_mode="diagonal", N=64)) == "tcgen05"
+    assert ssd.ssd_fwd_path(dims(a_mode="diagonal", N=64, Q=64, G=1, T=1)) == "tcgen05"
+    assert ssd.ssd_fwd_path(dims(a_mode="diagonal", N=128)) == "generic"
+    assert ssd.ssd_fwd_path(dims(a_mode="diagonal", N=64, P=32)) == "generic"
+    assert ssd.ssd_fwd_path(dims(a_mode="diagonal", N=64, dtype="f32")) == "generic"
+    with pytest.raises(ssd.SSDError) as e:
+        ssd.ssd_fwd_workspace_size(dims(a_mode="diagonal", N=128, path="tcgen05"))
+    assert e.value.status == ssd.SSD_ERR_UNSUPPORTED
+    # its workspace is the status block alone
+    assert ssd.ssd_fwd_workspace_size(dims(a_mode="diagonal", N=64, path="tcgen05")) == 256
+
+
 @pytest.mark.parametrize("big", [dict(H=70000, G=70000), dict(b=70000)], ids=["H_over_grid_y", "b_over_grid_z"])
 def test_dims_beyond_launch_limits_rejected_before_enqueue(lib, big):
     # The generic path's grids put H and b on grid dimensions y and z (at most 65535 each):
@@ -127,7 +141,7 @@ def test_dims_beyond_launch_limits_rejected_before_enqueue(lib, big):
         with pytest.raises(ssd.SSDError) as e:
             ssd.ssd_fwd_workspace_size(d)
         assert e.value.status == ssd.SSD_ERR_UNSUPPORTED
-    # diagonal A has no fused path, so AUTO has nothing to fall back to either
+    # diagonal A at N = 128 has no tcgen05 path, so AUTO has nothing to fall back to either
     with pytest.raises(ssd.SSDError) as e:
         ssd.ssd_fwd_workspace_size(dims(a_mode="diagonal", **big))
     assert e.value.status == ssd.SSD_ERR_UNSUPPORTED

@@ -1,6 +1,6 @@
 """GPU checks of the guards around the computation (through the C ABI).
 
-* fp16 range: the fused path's matrix operands are fp16; inputs (or states)
+* fp16 range: the tcgen05 paths' matrix operands are fp16; inputs (or states)
   beyond +-65504 must give either the oracle's answer or SSD_ERR_DEVICE from
   the device status -- never a silent inf/NaN with SSD_OK.
 * canaries: output and workspace buffers padded with sentinels on both sides;
@@ -34,15 +34,17 @@ BIG = [("x", 1e5), ("B", 1e5), ("C", 1e5), ("init_state", 1e5)]
 
 @pytest.mark.parametrize("what,val", BIG, ids=[b[0] for b in BIG])
 @pytest.mark.parametrize("path", ["tcgen05", "generic"])
-def test_out_of_fp16_range_is_reported_or_correct(what, val, path, cuda_device):
-    w = Workload("t", b=1, T=300, H=4, P=64, N=128, G=1, Q=128, D="none", init_std=0.1, seed=301)
+@pytest.mark.parametrize("a_mode", ["scalar", "diagonal"])
+def test_out_of_fp16_range_is_reported_or_correct(what, val, path, a_mode, cuda_device):
+    w = Workload("t", b=1, T=300, H=4, P=64, N=128 if a_mode == "scalar" else 64, G=1, Q=128,
+                 a_mode=a_mode, D="none", init_std=0.1, seed=301)
     inp = make_inputs(w)
     t = inp[what].clone()
     flat = t.view(-1)
     flat[[3, 777, flat.numel() // 2]] = val         # a few huge entries
     inp[what] = t
     d = {k: (None if v is None else v.to(cuda_device)) for k, v in inp.items()}
-    dims = ssd.make_dims(w.b, w.T, w.H, w.P, w.N, w.G, w.Q, path=path)
+    dims = ssd.make_dims(w.b, w.T, w.H, w.P, w.N, w.G, w.Q, a_mode=w.a_mode, path=path)
     ws = torch.empty(ssd.ssd_fwd_workspace_size(dims), device=cuda_device, dtype=torch.uint8)
     y, fin = _run(d, w, path, workspace=ws)
     st = ssd.ssd_check_device_status(ws)
@@ -64,11 +66,13 @@ def _padded(shape, dtype, dev, pad, fill):
 
 @pytest.mark.parametrize("T", [77, 300, 1000])
 @pytest.mark.parametrize("path", ["tcgen05", "generic"])
-def test_ragged_calls_stay_inside_their_buffers(T, path, cuda_device):
-    w = Workload("t", b=2, T=T, H=4, P=64, N=128, G=2, Q=128, D="normal", init_std=0.1, seed=400 + T)
+@pytest.mark.parametrize("a_mode", ["scalar", "diagonal"])
+def test_ragged_calls_stay_inside_their_buffers(T, path, a_mode, cuda_device):
+    w = Workload("t", b=2, T=T, H=4, P=64, N=128 if a_mode == "scalar" else 64, G=2, Q=128,
+                 a_mode=a_mode, D="normal", init_std=0.1, seed=400 + T)
     inp = make_inputs(w)
     d = {k: (None if v is None else v.to(cuda_device)) for k, v in inp.items()}
-    dims = ssd.make_dims(w.b, w.T, w.H, w.P, w.N, w.G, w.Q, path=path)
+    dims = ssd.make_dims(w.b, w.T, w.H, w.P, w.N, w.G, w.Q, a_mode=w.a_mode, path=path)
     need = ssd.ssd_fwd_workspace_size(dims)
     pad = 4096                                        # elements; keeps every view 16-byte aligned
     y_big, y = _padded((w.b, w.T, w.H, w.P), torch.bfloat16, cuda_device, pad, 7.0)
