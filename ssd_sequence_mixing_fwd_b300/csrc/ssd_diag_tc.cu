@@ -14,18 +14,19 @@
 //   h = exp(A Dt_end) o h_prev + sum_j (B_j o exp(A (Dt_end - Dt_j))) x_j^T
 //
 // The block's rows fall into eight 16-token groups; R_J is Dt at the last token
-// of group J (R_{-1} = 0) and M_J at its eighth token.  Every product is split
-// at a reference point between its two tokens, so that each factor carried by a
-// tensor-core operand is <= 1 (fp16 operands, fp32 accumulation):
+// of group J (R_{-1} = 0).  Every product is split at a reference point between
+// its two tokens, so that each factor carried by a tensor-core operand is <= 1
+// (fp16 operands, fp32 accumulation):
 //
 //  * S_ij, j in group J < group I of i: exp(A (Dt_i - R_J)) on the C side and
 //    exp(A (R_J - Dt_j)) on the B side.  The C side depends on J, so every row
 //    keeps one copy of its decayed C per earlier group -- written to TMEM, where
 //    the MMA takes it as its A operand -- and the seven products
 //    copy_J (128 x 64) x B~_J^T (64 x 16) fill S's columns group by group.
-//  * S_ij, j and i in the same group: on the CUDA cores in fp32, split at M_I
-//    (factors up to exp(|A| x half the group's Dt range); a group whose factors
-//    could leave fp32 takes one exponential per (i, j, n) instead).
+//  * S_ij, j and i in the same group: on the CUDA cores in fp32, split at the
+//    group's start R_{I-1} (the B side carries factors up to exp(|A| x the group's
+//    Dt range); a group whose factors could leave fp32 takes one exponential per
+//    (i, j, n) instead).
 //  * h_prev enters through C o exp(A Dt_i) (in TMEM) x h_prev (fp16, shared memory);
 //    the state's own product B o w (w <= 1) accumulates onto exp(A Dt_end) o h_prev,
 //    which the rows of the state rescale in place in TMEM.
@@ -33,14 +34,15 @@
 // The same map as the chunked algorithm of the other paths (equal up to
 // rounding); the block of 128 tokens plays the chunk's part whatever Q is.
 //
-// One CTA per (batch row, head) at a time (persistent over sequences), 6 warps:
+// One CTA per (batch row, head) at a time (persistent over sequences), 10 warps:
 //   warp 0      TMA producer: X, B, C tiles of a block (two stages)
 //   warp 1      TMEM owner; lane 0 issues every MMA
-//   warps 2-5   math: thread = TMEM lane = row i of the block (warp w owns lanes
-//               32 (w mod 4) ...); rows 0-63 also own the state rows n = i.
-// TMEM (512 columns): S 0-127 (fp32; its fp16 form overwrites columns 0-63 as it
-// is read), C copies 128-351 (7 x 32, fp16 pairs), C o exp(A Dt) 352-383, Y
-// 384-447, h 448-511 (lanes 0-63).
+//   warps 2-9   math, two per TMEM lane quarter: thread = TMEM lane = row i of the
+//               block (warp w owns lanes 32 (w mod 4) ...), the two warps of a quarter
+//               splitting the state dimension n (and the head dim p) in halves; rows
+//               0-63 also own the state rows n = i.
+// TMEM (512 columns): S 0-127 (fp32), C copies 128-351 (7 x 32, fp16 pairs; S in
+// fp16 then takes 128-191), C o exp(A Dt) 352-383, Y 384-447, h 448-511 (lanes 0-63).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -59,7 +61,8 @@ using namespace ptx;
 constexpr int kBlk = 128;          // tokens per block
 constexpr int kP = 64;             // head dim of this path
 constexpr int kN = 64;             // state dim of this path
-constexpr int kThreads = 192;      // 6 warps
+constexpr int kThreads = 320;      // 10 warps
+constexpr int kMathWarps = 8;
 constexpr int kTile = 128 * 128;   // 128 rows x 64 16-bit values
 
 // shared memory (byte offsets from a 1024-aligned base)
@@ -67,30 +70,33 @@ constexpr int kStageBytes = 3 * kTile;                 // X, B, C (bf16 as loade
 constexpr int kOffStage = 0;                           // [2 stages]
 constexpr int kOffBt = 2 * kStageBytes;                // B~ (fp16, [j][n], 128B swizzle)
 constexpr int kOffBw = kOffBt + kTile;                 // B o w (fp16, [j][n])
-constexpr int kOffBp = kOffBw + kTile;                 // B' (fp32, [j][64]) for the diagonal groups
+constexpr int kOffBp = kOffBw + kTile;                 // B' (fp32, [j][64], row-swizzled 16-byte chunks)
 constexpr int kOffHp = kOffBp + 2 * kTile;             // h_prev (fp16, [n][p])
-constexpr int kOffY = kOffHp + 64 * 128;               // y: [4 warps][32 rows][128 B]
-constexpr int kTabRow = 68;                            // floats per table row (64 + bank padding)
-constexpr int kTabRows = 22;                           // per warp: T1 T2 T3 T5 x 2 groups, G x 2 groups x 7
+constexpr int kOffY = kOffHp + 64 * 128;               // y: [4 quarters][32 rows][128 B]
+constexpr int kTabRow = 36;                            // floats per table row (32 + bank padding)
+constexpr int kTabRows = 20;                           // per warp: T2 T3 g x 2 groups, G x 2 groups x 7
 constexpr int kTabWarpBytes = kTabRows * kTabRow * 4;
-constexpr int kOffTab = kOffY + kTile;                 // per-warp tables
-constexpr int kOffDtW = kOffTab + 4 * kTabWarpBytes;   // per-warp Dt of all 128 rows
-constexpr int kOffA2 = kOffDtW + 4 * 512;              // per-warp A (log2 units), 64 floats
-constexpr int kOffMisc = kOffA2 + 4 * 256;             // TMEM base, abort flag
+constexpr int kOffTab = kOffY + kTile;                 // per math warp: tables of its n half
+constexpr int kDpRow = 20;                             // floats per row of the partial sums (16 + padding)
+constexpr int kOffDp = kOffTab + kMathWarps * kTabWarpBytes;   // [128][kDpRow] partial diagonal-group sums
+constexpr int kOffDtW = kOffDp + 128 * kDpRow * 4;     // per math warp: Dt of all 128 rows
+constexpr int kOffA2 = kOffDtW + kMathWarps * 512;     // per math warp: A (log2 units) of its n half
+constexpr int kOffMisc = kOffA2 + kMathWarps * 128;    // TMEM base, abort flag
 constexpr int kOffBar = kOffMisc + 16;
 constexpr int kNumBars = 8;
 constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 1024;   // + alignment slack
+static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
 constexpr int B_FULL = 0;     // [2] TMA landed a stage
-constexpr int B_EMPTY = 2;    // [2] the math warps are done with a stage (4 warps)
-constexpr int B_OPS = 4;      // operands of a block written (4 warps)
+constexpr int B_EMPTY = 2;    // [2] the math warps are done with a stage (8 warps)
+constexpr int B_OPS = 4;      // operands of a block written (8 warps)
 constexpr int B_SFULL = 5;    // S, Y_off and the state product are done
-constexpr int B_S16 = 6;      // S (fp16) written (4 warps)
+constexpr int B_S16 = 6;      // S (fp16) written (8 warps)
 constexpr int B_YFULL = 7;    // S X is done
 
 constexpr uint32_t kTmS = 0;
-constexpr uint32_t kTmS16 = 0;
 constexpr uint32_t kTmCp = 128;
+constexpr uint32_t kTmS16 = 128;
 constexpr uint32_t kTmCh = 352;
 constexpr uint32_t kTmY = 384;
 constexpr uint32_t kTmH = 448;
@@ -105,23 +111,29 @@ struct DiagParams {
     int b, T, H, G, nblk, nseq;
 };
 
-// The diagonal group of a row whose split factors could leave fp32: S_ij =
-// sum_n C_in B_jn exp(A_n (Dt_i - Dt_j)) with one exponential per term (C from the
+// 16-byte chunk c of row r of the B' table sits at chunk c ^ bp_swz(r): eight consecutive
+// rows (one warp's stores) spread over all banks, and rows r and r + 16 (the rows two
+// halves of a warp read at once) land in different banks.
+__device__ __forceinline__ int bp_swz(int r) { return (r ^ (r >> 4)) & 7; }
+
+// The diagonal group of a row whose split factors could leave fp32, over one half of n:
+// sum_{n in half} C_in B_jn exp(A_n (Dt_i - Dt_j)) with one exponential per term (C from the
 // row's tile, B from the B' table, which holds B itself for such a group).
 static __device__ __noinline__ void diag_group_direct(const unsigned char *crow, uint32_t rx, const float *Bp,
-                                                      const float *A2s, const float *DtW, int i, float *d) {
-    const int I = i >> 4, sw = I & 1;
+                                                      const float *A2h, const float *DtW, int i, int hn,
+                                                      float *d) {
+    const int I = i >> 4;
     const float Dti = DtW[i];
-    float c[64];
+    float c[32];
 #pragma unroll
-    for (int cc = 0; cc < 8; ++cc) {
-        const uint4 w = *reinterpret_cast<const uint4 *>(crow + ((16u * cc) ^ rx));
+    for (int k = 0; k < 4; ++k) {
+        const uint4 w = *reinterpret_cast<const uint4 *>(crow + ((16u * (4 * hn + k)) ^ rx));
         const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const float2 f = bf2_to_f2(ws[e]);
-            c[8 * cc + 2 * e] = f.x;
-            c[8 * cc + 2 * e + 1] = f.y;
+            c[8 * k + 2 * e] = f.x;
+            c[8 * k + 2 * e + 1] = f.y;
         }
     }
     for (int jj = 0; jj < 16; ++jj) {
@@ -130,17 +142,19 @@ static __device__ __noinline__ void diag_group_direct(const unsigned char *crow,
         const float dd = Dti - DtW[j];
         float s0 = 0.f;
 #pragma unroll
-        for (int c4 = 0; c4 < 16; ++c4) {
-            const float4 bv = brow[c4 ^ sw];
+        for (int c4 = 0; c4 < 8; ++c4) {
+            const float4 bv = brow[(8 * hn + c4) ^ bp_swz(j)];
             const int n = 4 * c4;
-            s0 = fmaf(c[n] * bv.x, ex2(A2s[n] * dd), s0);
-            s0 = fmaf(c[n + 1] * bv.y, ex2(A2s[n + 1] * dd), s0);
-            s0 = fmaf(c[n + 2] * bv.z, ex2(A2s[n + 2] * dd), s0);
-            s0 = fmaf(c[n + 3] * bv.w, ex2(A2s[n + 3] * dd), s0);
+            s0 = fmaf(c[n] * bv.x, ex2(A2h[n] * dd), s0);
+            s0 = fmaf(c[n + 1] * bv.y, ex2(A2h[n + 1] * dd), s0);
+            s0 = fmaf(c[n + 2] * bv.z, ex2(A2h[n + 2] * dd), s0);
+            s0 = fmaf(c[n + 3] * bv.w, ex2(A2h[n + 3] * dd), s0);
         }
         d[jj] = jj <= (i & 15) ? s0 : 0.f;
     }
 }
+
+__device__ __forceinline__ void pair_sync(int q) { asm volatile("bar.sync %0, 64;" ::"r"(1 + q) : "memory"); }
 
 __global__ void __launch_bounds__(kThreads, 1)
     ssd_diag_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_B,
@@ -160,11 +174,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 0;
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar(B_FULL + s), 1);
-            mbar_init(bar(B_EMPTY + s), 4);
+            mbar_init(bar(B_EMPTY + s), kMathWarps);
         }
-        mbar_init(bar(B_OPS), 4);
+        mbar_init(bar(B_OPS), kMathWarps);
         mbar_init(bar(B_SFULL), 1);
-        mbar_init(bar(B_S16), 4);
+        mbar_init(bar(B_S16), kMathWarps);
         mbar_init(bar(B_YFULL), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -250,54 +264,62 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------------------ math warps
         const int q = warp & 3;                     // TMEM lane quarter
+        const int hn = (warp - 2) >> 2;             // which half of n (and of p) this warp takes
         const int i = 32 * q + lane;                // row of the block (token / state row)
         const int I = i >> 4;                       // 16-row group
         const int lg = (lane >> 4) & 1;             // the group's index within this warp
+        const bool need_d = hn == (q < 2 ? 0 : 1);  // this warp's S columns hold the diagonal group
         const uint32_t lane_off = (uint32_t)(32 * q) << 16;
-        float *tab = reinterpret_cast<float *>(smem + kOffTab + q * kTabWarpBytes);
-        float *DtW = reinterpret_cast<float *>(smem + kOffDtW + q * 512);
-        float *A2s = reinterpret_cast<float *>(smem + kOffA2 + q * 256);
+        float *tab = reinterpret_cast<float *>(smem + kOffTab + (warp - 2) * kTabWarpBytes);
+        float *DtW = reinterpret_cast<float *>(smem + kOffDtW + (warp - 2) * 512);
+        float *A2h = reinterpret_cast<float *>(smem + kOffA2 + (warp - 2) * 128);
         float *Bp = reinterpret_cast<float *>(smem + kOffBp);
+        float *Dp = reinterpret_cast<float *>(smem + kOffDp) + i * kDpRow;
         unsigned char *ybuf = smem + kOffY + q * 4096;
         const uint32_t ybuf_a = sbase + kOffY + q * 4096;
-        // Every table factor lies in (0, 1]; those that multiply a factor above 1 (T1, T5) are
-        // at least 2^-110 in a group within the split's range, so no product underflows
-        // unless its exact value is below fp32's normal range.
-        auto T1 = [&](int n) -> float & { return tab[(0 + lg) * kTabRow + n]; };   // exp(A (M_I - R_{I-1}))
-        auto T2 = [&](int n) -> float & { return tab[(2 + lg) * kTabRow + n]; };   // exp(A R_{I-1})
-        auto T3 = [&](int n) -> float & { return tab[(4 + lg) * kTabRow + n]; };   // exp(A (Dt_end - R_I))
-        auto T5 = [&](int n) -> float & { return tab[(6 + lg) * kTabRow + n]; };   // exp(A (R_I - M_I))
-        auto Gt = [&](int J, int n) -> float & { return tab[(8 + 7 * lg + J) * kTabRow + n]; };  // exp(A (R_{I-1} - R_J))
+        // Per-warp tables over this warp's half of n, each factor in (0, 1]:
+        //   T2 = exp(A R_{I-1}), T3 = exp(A (Dt_end - R_I)), g = exp(A (R_I - R_{I-1})) for the
+        //   warp's two groups, and G_J = exp(A (R_{I-1} - R_J)) for every earlier group J.
+        // g multiplies a factor up to exp(|A| (R_I - R_{I-1})) and is at least 2^-110 in a
+        // group within the split's range, so no product underflows unless its exact value is
+        // below fp32's normal range.
+        auto T2 = [&](int k) { return reinterpret_cast<const float4 *>(tab + (0 + lg) * kTabRow)[k >> 2]; };
+        auto T3 = [&](int k) { return reinterpret_cast<const float4 *>(tab + (2 + lg) * kTabRow)[k >> 2]; };
+        auto Tg = [&](int k) { return reinterpret_cast<const float4 *>(tab + (4 + lg) * kTabRow)[k >> 2]; };
+        auto Gt = [&](int J, int k) { return reinterpret_cast<const float4 *>(tab + (6 + 7 * lg + J) * kTabRow)[k >> 2]; };
+        auto A4 = [&](int k) { return reinterpret_cast<const float4 *>(A2h)[k >> 2]; };
         uint32_t bad = 0;
         int kb = 0;
         for (int sq = blockIdx.x; sq < p.nseq; sq += gridDim.x) {
             const int bi = sq / p.H, h = sq - bi * p.H;
             __syncwarp();
-            const float a0 = p.A[(int64_t)h * kN + lane] * kLog2e, a1 = p.A[(int64_t)h * kN + 32 + lane] * kLog2e;
-            A2s[lane] = a0;
-            A2s[32 + lane] = a1;
-            float amax = fmaxf(fabsf(a0), fabsf(a1));
+            const float an_own = p.A[(int64_t)h * kN + 32 * hn + lane] * kLog2e;   // n = 32 hn + lane
+            A2h[lane] = an_own;
+            float amax = fabsf(an_own);
 #pragma unroll
             for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            // the split's range check uses |A| over all n (the other half from the other warp's values)
+            const float amax_other = fabsf(p.A[(int64_t)h * kN + 32 * (1 - hn) + lane]) * kLog2e;
+            float am2 = amax_other;
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) am2 = fmaxf(am2, __shfl_xor_sync(0xffffffffu, am2, o));
+            amax = fmaxf(amax, am2);
+            const float a_row = q < 2 ? p.A[(int64_t)h * kN + i] * kLog2e : 0.f;   // state row n = i
             const float Dh = p.D ? p.D[h] : 0.f;
             __syncwarp();
-            // the initial state into TMEM (state rows 0-63: quarters 0 and 1)
+            // the initial state into TMEM (state rows 0-63: quarters 0 and 1; this warp's half of p)
             if (q < 2) {
+                float v[32];
+                const float *src = p.init ? p.init + ((int64_t)sq * kN + i) * kP + 32 * hn : nullptr;
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    float v[32];
-                    const float *src = p.init ? p.init + ((int64_t)sq * kN + i) * kP + 32 * half : nullptr;
-#pragma unroll
-                    for (int e = 0; e < 32; e += 4) {
-                        const float4 f = src ? __ldg(reinterpret_cast<const float4 *>(src + e))
-                                             : make_float4(0.f, 0.f, 0.f, 0.f);
-                        v[e] = f.x;
-                        v[e + 1] = f.y;
-                        v[e + 2] = f.z;
-                        v[e + 3] = f.w;
-                    }
-                    tmem_st32(tmem + lane_off + kTmH + 32 * half, v);
+                for (int e = 0; e < 32; e += 4) {
+                    const float4 f = src ? __ldg(reinterpret_cast<const float4 *>(src + e)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    v[e] = f.x;
+                    v[e + 1] = f.y;
+                    v[e + 2] = f.z;
+                    v[e + 3] = f.w;
                 }
+                tmem_st32(tmem + lane_off + kTmH + 32 * hn, v);
                 tmem_st_wait();
             }
             auto load_dt = [&](int c, float (&v)[4]) {
@@ -309,10 +331,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             float dtn[4];
             load_dt(0, dtn);
-            for (int c = 0; c < p.nblk; ++c, ++kb) {
-                const int st = kb & 1;
-                // (1) Dt: inclusive prefix sums of dt over the block (four interleaved 32-row
-                // scans; every warp computes all 128 rows), the warp's tables
+            // (1) + (2) of a block, run for block c + 1 while block c's S X is in flight:
+            // Dt, the inclusive prefix sums of dt over the block (four interleaved 32-row scans;
+            // every warp computes all 128 rows), the warp's tables, and the state rows' h_prev
+            // (fp16, for (C o e) h_prev) and rescaling h <- exp(A Dt_end) o h in place (the state
+            // product of the previous block, which wrote h, and (C o e) h_prev, which read the
+            // h_prev tile, have completed)
+            float Dti = 0.f, Dend = 0.f, RI = 0.f, Rm1 = 0.f;
+            bool safe = true;
+            auto prep = [&](int c) {
                 float Dv[4];
 #pragma unroll
                 for (int m = 0; m < 4; ++m) Dv[m] = dtn[m];
@@ -334,107 +361,97 @@ __global__ void __launch_bounds__(kThreads, 1)
                         run += tot;
                     }
                 }
+                __syncwarp();
 #pragma unroll
                 for (int m = 0; m < 4; ++m) DtW[32 * m + lane] = Dv[m];
                 __syncwarp();
-                const float Dti = DtW[i];
-                const float Dend = DtW[127];
-                const float RI = DtW[16 * I + 15], MI = DtW[16 * I + 7];
-                const float Rm1 = I > 0 ? DtW[16 * I - 1] : 0.f;
-                const bool safe = amax * fmaxf(MI - Rm1, RI - MI) <= kSafeLog2;
-                // tables of this warp's two groups: T1, T2, T3, T5 and G (per earlier group J)
+                Dti = DtW[i];
+                Dend = DtW[127];
+                RI = DtW[16 * I + 15];
+                Rm1 = I > 0 ? DtW[16 * I - 1] : 0.f;
+                // pairs inside the group are split at the group's start: factors up to
+                // exp2(|A| (R_I - R_{I-1})) on the B side
+                safe = amax * (RI - Rm1) <= kSafeLog2;
 #pragma unroll
-                for (int hn = 0; hn < 2; ++hn) {
-                    const int n = lane + 32 * hn;
-                    const float an = hn ? a1 : a0;
+                for (int l2 = 0; l2 < 2; ++l2) {
+                    const int I2 = 2 * q + l2;
+                    const float r1 = I2 > 0 ? DtW[16 * I2 - 1] : 0.f;
+                    const float r2 = DtW[16 * I2 + 15];
+                    tab[(0 + l2) * kTabRow + lane] = ex2(an_own * r1);
+                    tab[(2 + l2) * kTabRow + lane] = ex2(an_own * (Dend - r2));
+                    tab[(4 + l2) * kTabRow + lane] = ex2(an_own * (r2 - r1));
 #pragma unroll
-                    for (int l2 = 0; l2 < 2; ++l2) {
-                        const int I2 = 2 * q + l2;
-                        const float r1 = I2 > 0 ? DtW[16 * I2 - 1] : 0.f;
-                        const float m2 = DtW[16 * I2 + 7], r2 = DtW[16 * I2 + 15];
-                        tab[(0 + l2) * kTabRow + n] = ex2(an * (m2 - r1));
-                        tab[(2 + l2) * kTabRow + n] = ex2(an * r1);
-                        tab[(4 + l2) * kTabRow + n] = ex2(an * (Dend - r2));
-                        tab[(6 + l2) * kTabRow + n] = ex2(an * (r2 - m2));
-                    }
-#pragma unroll
-                    for (int l2 = 0; l2 < 2; ++l2) {
-                        const int I2 = 2 * q + l2;
-                        const float r1 = I2 > 0 ? DtW[16 * I2 - 1] : 0.f;
-                        for (int J = 0; J < I2; ++J) tab[(8 + 7 * l2 + J) * kTabRow + n] = ex2(an * (r1 - DtW[16 * J + 15]));
-                    }
+                    for (int J = 0; J < 7; ++J)
+                        if (J < I2) tab[(6 + 7 * l2 + J) * kTabRow + lane] = ex2(an_own * (r1 - DtW[16 * J + 15]));
                 }
                 __syncwarp();
-
-                // (2) state rows: h_prev (fp16) for (C o e) h_prev; h <- exp(A Dt_end) o h in place
                 if (q < 2) {
-                    const float an = ex2(A2s[i] * Dend);
+                    const float an = ex2(a_row * Dend);
                     unsigned char *hrow = smem + kOffHp + i * 128;
-                    const uint32_t rx = (uint32_t)(i & 7) * 16u;
+                    const uint32_t rxh = (uint32_t)(i & 7) * 16u;
+                    float hv[32];
+                    tmem_ld32(tmem + lane_off + kTmH + 32 * hn, hv);
+                    tmem_ld_wait();
 #pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        float hv[32];
-                        tmem_ld32(tmem + lane_off + kTmH + 32 * half, hv);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int cc = 0; cc < 4; ++cc) {
-                            const int e = 8 * cc;
-                            *reinterpret_cast<uint4 *>(hrow + ((16u * (4 * half + cc)) ^ rx)) =
-                                make_uint4(pack_h2(hv[e], hv[e + 1]), pack_h2(hv[e + 2], hv[e + 3]),
-                                           pack_h2(hv[e + 4], hv[e + 5]), pack_h2(hv[e + 6], hv[e + 7]));
-                        }
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) hv[e] *= an;
-                        tmem_st32(tmem + lane_off + kTmH + 32 * half, hv);
+                    for (int cc = 0; cc < 4; ++cc) {
+                        const int e = 8 * cc;
+                        *reinterpret_cast<uint4 *>(hrow + ((16u * (4 * hn + cc)) ^ rxh)) =
+                            make_uint4(pack_h2(hv[e], hv[e + 1]), pack_h2(hv[e + 2], hv[e + 3]),
+                                       pack_h2(hv[e + 4], hv[e + 5]), pack_h2(hv[e + 6], hv[e + 7]));
                     }
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) hv[e] *= an;
+                    tmem_st32(tmem + lane_off + kTmH + 32 * hn, hv);
                 }
+            };
+            prep(0);
+            for (int c = 0; c < p.nblk; ++c, ++kb) {
+                const int st = kb & 1;
 
-                // (3) operands of row i
+                // (3) operands of row i, this warp's half of n (16-byte chunks 4 hn .. 4 hn + 3)
                 wait_bar(ctl, bar(B_FULL + st), (kb >> 1) & 1);
                 unsigned char *xt = smem + kOffStage + st * kStageBytes;
                 const uint32_t rx = (uint32_t)(i & 7) * 16u;
                 {
                     // X: bf16 -> fp16 in place; D x into Y's columns (Y_off accumulates onto it)
                     unsigned char *row = xt + i * 128;
-                    uint4 u[8];
+                    uint4 u[4];
 #pragma unroll
-                    for (int cc = 0; cc < 8; ++cc) u[cc] = *reinterpret_cast<const uint4 *>(row + ((16u * cc) ^ rx));
+                    for (int k = 0; k < 4; ++k) u[k] = *reinterpret_cast<const uint4 *>(row + ((16u * (4 * hn + k)) ^ rx));
                     if (p.D) {
+                        float dx[32];
 #pragma unroll
-                        for (int half = 0; half < 2; ++half) {
-                            float dx[32];
+                        for (int k = 0; k < 4; ++k) {
+                            const uint32_t ws[4] = {u[k].x, u[k].y, u[k].z, u[k].w};
 #pragma unroll
-                            for (int cc = 0; cc < 4; ++cc) {
-                                const uint4 w = u[4 * half + cc];
-                                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    const float2 f = bf2_to_f2(ws[e]);
-                                    dx[8 * cc + 2 * e] = Dh * f.x;
-                                    dx[8 * cc + 2 * e + 1] = Dh * f.y;
-                                }
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 f = bf2_to_f2(ws[e]);
+                                dx[8 * k + 2 * e] = Dh * f.x;
+                                dx[8 * k + 2 * e + 1] = Dh * f.y;
                             }
-                            tmem_st32(tmem + lane_off + kTmY + 32 * half, dx);
                         }
+                        tmem_st32(tmem + lane_off + kTmY + 32 * hn, dx);
                     }
 #pragma unroll
-                    for (int cc = 0; cc < 8; ++cc) {
-                        u[cc].x = bf2_to_h2(u[cc].x);
-                        u[cc].y = bf2_to_h2(u[cc].y);
-                        u[cc].z = bf2_to_h2(u[cc].z);
-                        u[cc].w = bf2_to_h2(u[cc].w);
-                        *reinterpret_cast<uint4 *>(row + ((16u * cc) ^ rx)) = u[cc];
+                    for (int k = 0; k < 4; ++k) {
+                        u[k].x = bf2_to_h2(u[k].x);
+                        u[k].y = bf2_to_h2(u[k].y);
+                        u[k].z = bf2_to_h2(u[k].z);
+                        u[k].w = bf2_to_h2(u[k].w);
+                        *reinterpret_cast<uint4 *>(row + ((16u * (4 * hn + k)) ^ rx)) = u[k];
                     }
                 }
                 {
-                    // B: B' = B exp(A (M_I - Dt_i)) (fp32, for the diagonal group), B~ = B' T5 =
+                    // B: B' = B exp(A (R_{I-1} - Dt_i)) (fp32, for the diagonal group), B~ = B' g =
                     // B exp(A (R_I - Dt_i)), B o w = B~ T3 = B exp(A (Dt_end - Dt_i)) (fp16); a group
                     // outside the split's range keeps B itself in B' and forms B~ directly
                     const unsigned char *row = xt + kTile + i * 128;
                     float *bprow = Bp + i * 64;
-                    const int sw = I & 1;
-#pragma unroll 2
-                    for (int cc = 0; cc < 8; ++cc) {
+                    const int bsw = bp_swz(i);
+                    const float bref = safe ? Rm1 : RI;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int cc = 4 * hn + k;
                         const uint4 w = *reinterpret_cast<const uint4 *>(row + ((16u * cc) ^ rx));
                         const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
                         float bv[8], bt[8], bw[8];
@@ -445,64 +462,67 @@ __global__ void __launch_bounds__(kThreads, 1)
                             bv[2 * e + 1] = f.y;
                         }
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const int n = 8 * cc + e;
-                            const float an = A2s[n];
-                            if (safe) {
-                                const float b1 = bv[e] * ex2(an * (MI - Dti));
-                                bt[e] = b1 * T5(n);
-                                bv[e] = b1;
-                            } else {
-                                bt[e] = bv[e] * ex2(an * (RI - Dti));
+                        for (int h4 = 0; h4 < 2; ++h4) {
+                            const int k0 = 8 * k + 4 * h4;       // n - 32 hn
+                            const float4 a4 = A4(k0), g4 = Tg(k0), t4 = T3(k0);
+                            const float av[4] = {a4.x, a4.y, a4.z, a4.w}, gv[4] = {g4.x, g4.y, g4.z, g4.w},
+                                        tv[4] = {t4.x, t4.y, t4.z, t4.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int m = 4 * h4 + e;
+                                const float b1 = bv[m] * ex2(av[e] * (bref - Dti));
+                                bt[m] = safe ? b1 * gv[e] : b1;
+                                bw[m] = bt[m] * tv[e];
+                                if (safe) bv[m] = b1;
                             }
-                            bw[e] = bt[e] * T3(n);
                         }
-                        *reinterpret_cast<float4 *>(bprow + 4 * ((2 * cc) ^ sw)) = make_float4(bv[0], bv[1], bv[2], bv[3]);
-                        *reinterpret_cast<float4 *>(bprow + 4 * ((2 * cc + 1) ^ sw)) = make_float4(bv[4], bv[5], bv[6], bv[7]);
+                        *reinterpret_cast<float4 *>(bprow + 4 * ((2 * cc) ^ bsw)) = make_float4(bv[0], bv[1], bv[2], bv[3]);
+                        *reinterpret_cast<float4 *>(bprow + 4 * ((2 * cc + 1) ^ bsw)) = make_float4(bv[4], bv[5], bv[6], bv[7]);
                         *reinterpret_cast<uint4 *>(smem + kOffBt + i * 128 + ((16u * cc) ^ rx)) =
                             make_uint4(pack_h2(bt[0], bt[1]), pack_h2(bt[2], bt[3]), pack_h2(bt[4], bt[5]), pack_h2(bt[6], bt[7]));
                         *reinterpret_cast<uint4 *>(smem + kOffBw + i * 128 + ((16u * cc) ^ rx)) =
                             make_uint4(pack_h2(bw[0], bw[1]), pack_h2(bw[2], bw[3]), pack_h2(bw[4], bw[5]), pack_h2(bw[6], bw[7]));
                     }
                 }
-                // C: C' = C exp(A (Dt_i - M_I)) (fp32, kept for the diagonal group); the C side
-                // of everything else is C' T1 = C exp(A (Dt_i - R_{I-1})) <= 1 times a table
-                // factor.  (C' T1 is formed before the next factor, never T1 times that factor:
-                // C' may be large where the product is not small.)  A group outside the split's
-                // range takes C exp(A (Dt_i - R_{I-1})) directly (and its diagonal group later
-                // reads C from the tile).
-                float cr[64];
+                // C: C~ = C exp(A (Dt_i - R_{I-1})) <= 1 (at least 2^-110 x C in a group within the
+                // split's range): the diagonal group's C side as it is, the C side of everything
+                // else times a table factor
+                float cr[32];
                 {
                     const unsigned char *row = xt + 2 * kTile + i * 128;
-                    const float ref = safe ? MI : Rm1;
-                    uint32_t wh[32];
+                    uint32_t wh[16];
 #pragma unroll
-                    for (int cc = 0; cc < 8; ++cc) {
-                        const uint4 w = *reinterpret_cast<const uint4 *>(row + ((16u * cc) ^ rx));
+                    for (int k = 0; k < 4; ++k) {
+                        const uint4 w = *reinterpret_cast<const uint4 *>(row + ((16u * (4 * hn + k)) ^ rx));
+                        const float4 a4a = A4(8 * k), a4b = A4(8 * k + 4);
+                        const float av[8] = {a4a.x, a4a.y, a4a.z, a4a.w, a4b.x, a4b.y, a4b.z, a4b.w};
                         const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const float2 f = bf2_to_f2(ws[e]);
-                            const int n = 8 * cc + 2 * e;
-                            cr[n] = f.x * ex2(A2s[n] * (Dti - ref));
-                            cr[n + 1] = f.y * ex2(A2s[n + 1] * (Dti - ref));
+                            const int m = 8 * k + 2 * e;
+                            cr[m] = f.x * ex2(av[2 * e] * (Dti - Rm1));
+                            cr[m + 1] = f.y * ex2(av[2 * e + 1] * (Dti - Rm1));
                         }
                     }
-                    auto t1 = [&](int n) -> float { return safe ? T1(n) : 1.f; };
 #pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        wh[e] = pack_h2((cr[2 * e] * t1(2 * e)) * T2(2 * e), (cr[2 * e + 1] * t1(2 * e + 1)) * T2(2 * e + 1));
-                    tmem_st32u(tmem + lane_off + kTmCh, wh);
-                    // one copy per earlier group J: C exp(A (Dt_i - R_J)) = C' T1 G_J; copies J >= I
-                    // of a row are never read (those columns of S are replaced), so they are zeros
+                    for (int k4 = 0; k4 < 8; ++k4) {
+                        const float4 t = T2(4 * k4);
+                        wh[2 * k4] = pack_h2(cr[4 * k4] * t.x, cr[4 * k4 + 1] * t.y);
+                        wh[2 * k4 + 1] = pack_h2(cr[4 * k4 + 2] * t.z, cr[4 * k4 + 3] * t.w);
+                    }
+                    tmem_st16(tmem + lane_off + kTmCh + 16 * hn, wh);
+                    // one copy per earlier group J: C exp(A (Dt_i - R_J)) = C~ G_J; copies J >= I
+                    // of a row are never read (those columns of S are replaced): zeros
                     for (int J = 0; J <= 2 * q; ++J) {
-                        const bool use = J <= I - 1;
+                        const float z = J <= I - 1 ? 1.f : 0.f;
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            const float g0 = use ? Gt(J, 2 * e) : 0.f, g1 = use ? Gt(J, 2 * e + 1) : 0.f;
-                            wh[e] = pack_h2((cr[2 * e] * t1(2 * e)) * g0, (cr[2 * e + 1] * t1(2 * e + 1)) * g1);
+                        for (int k4 = 0; k4 < 8; ++k4) {
+                            const float4 t = Gt(J, 4 * k4);
+                            wh[2 * k4] = pack_h2(cr[4 * k4] * (t.x * z), cr[4 * k4 + 1] * (t.y * z));
+                            wh[2 * k4 + 1] = pack_h2(cr[4 * k4 + 2] * (t.z * z), cr[4 * k4 + 3] * (t.w * z));
                         }
-                        tmem_st32u(tmem + lane_off + kTmCp + 32 * J, wh);
+                        tmem_st16(tmem + lane_off + kTmCp + 32 * J + 16 * hn, wh);
                     }
                 }
                 tmem_st_wait();
@@ -511,40 +531,63 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(B_OPS));
 
-                // (4) the diagonal group: S_ij = sum_n C'_in B'_jn, j <= i (fp32; while the MMAs run)
+                // (4) the diagonal group over this warp's half of n: S_ij = sum_n C~_in B'_jn,
+                // j <= i (fp32; while the MMAs run), two rows j at a time.  The B' rows of the
+                // group were written by this warp and its partner: the pair barrier below orders
+                // them (and the partner's partial sums) before their use.
+                pair_sync(q);
                 float d[16];
                 if (safe) {
-                    const int sw = I & 1;
 #pragma unroll
                     for (int jj = 0; jj < 16; ++jj) {
-                        const float4 *brow = reinterpret_cast<const float4 *>(Bp + (16 * I + jj) * 64);
+                        const int j0 = 16 * I + jj;
+                        const float4 *b0 = reinterpret_cast<const float4 *>(Bp + j0 * 64);
+                        const int s0w = bp_swz(j0) ^ (8 * hn);
                         float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
-                        for (int c4 = 0; c4 < 16; ++c4) {
-                            const float4 bv = brow[c4 ^ sw];
-                            s0 = fmaf(cr[4 * c4], bv.x, s0);
-                            s1 = fmaf(cr[4 * c4 + 1], bv.y, s1);
-                            s2 = fmaf(cr[4 * c4 + 2], bv.z, s2);
-                            s3 = fmaf(cr[4 * c4 + 3], bv.w, s3);
+                        for (int c4 = 0; c4 < 8; ++c4) {
+                            const float4 v0 = b0[c4 ^ s0w];
+                            s0 = fmaf(cr[4 * c4], v0.x, s0);
+                            s1 = fmaf(cr[4 * c4 + 1], v0.y, s1);
+                            s2 = fmaf(cr[4 * c4 + 2], v0.z, s2);
+                            s3 = fmaf(cr[4 * c4 + 3], v0.w, s3);
                         }
                         d[jj] = jj <= (i & 15) ? (s0 + s1) + (s2 + s3) : 0.f;
                     }
                 } else {
                     float dl[16];
-                    diag_group_direct(xt + 2 * kTile + i * 128, rx, Bp, A2s, DtW, i, dl);
+                    diag_group_direct(xt + 2 * kTile + i * 128, rx, Bp, A2h, DtW, i, hn, dl);
 #pragma unroll
                     for (int jj = 0; jj < 16; ++jj) d[jj] = dl[jj];
                 }
+                // the partner that does not merge the diagonal group hands over its partial sums;
+                // the y store of the previous block has read the quarter's buffer by the same barrier
+                if (!need_d) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        *reinterpret_cast<float4 *>(Dp + 4 * k) = make_float4(d[4 * k], d[4 * k + 1], d[4 * k + 2], d[4 * k + 3]);
+                }
+                if (hn == 0 && lane == 0) bulk_wait_read0();
+                pair_sync(q);
+                if (need_d) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float4 o = *reinterpret_cast<const float4 *>(Dp + 4 * k);
+                        d[4 * k] += o.x;
+                        d[4 * k + 1] += o.y;
+                        d[4 * k + 2] += o.z;
+                        d[4 * k + 3] += o.w;
+                    }
+                }
 
                 // (5) S: the copies' products left of the diagonal group, the diagonal group,
-                // zeros right of it -> fp16 over S's first 64 columns (each chunk of 16 written
-                // columns lies in columns already read)
+                // zeros right of it -> fp16 (this warp: S columns 64 hn .. 64 hn + 63)
                 wait_bar(ctl, bar(B_SFULL), kb & 1);
                 tc_fence_after();
-#pragma unroll
-                for (int k4 = 0; k4 < 4; ++k4) {
+#pragma unroll 1
+                for (int k2 = 0; k2 < 2; ++k2) {
                     float sv[32];
-                    tmem_ld32(tmem + lane_off + kTmS + 32 * k4, sv);
+                    tmem_ld32(tmem + lane_off + kTmS + 64 * hn + 32 * k2, sv);
                     tmem_ld_wait();
                     uint32_t w[16];
 #pragma unroll
@@ -552,28 +595,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                         float v2[2];
 #pragma unroll
                         for (int u = 0; u < 2; ++u) {
-                            const int j = 32 * k4 + 2 * e + u;
-                            const int Jg = j >> 4;
-                            v2[u] = Jg < I ? sv[2 * e + u] : (Jg == I ? d[j & 15] : 0.f);
+                            const int col = 32 * k2 + 2 * e + u;          // within this warp's 64 columns
+                            const int Jg = 4 * hn + (col >> 4);
+                            v2[u] = Jg < I ? sv[2 * e + u] : (Jg == I ? d[col & 15] : 0.f);
                         }
                         w[e] = pack_h2(v2[0], v2[1]);
                     }
-                    tmem_st16(tmem + lane_off + kTmS16 + 16 * k4, w);
+                    tmem_st16(tmem + lane_off + kTmS16 + 32 * hn + 16 * k2, w);
                 }
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(B_S16));
+                if (c + 1 < p.nblk) prep(c + 1);
 
-                // (6) epilogue: y = Y (bf16) -> this warp's 32-row buffer -> TMA store
+                // (6) epilogue: y = Y (bf16; this warp: columns 32 hn ..) -> the quarter's 32-row
+                // buffer -> TMA store
                 wait_bar(ctl, bar(B_YFULL), kb & 1);
                 tc_fence_after();
-                if (lane == 0) bulk_wait_read0();   // this warp's previous store has read its buffer
-                __syncwarp();
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
+                {
                     float yv[32];
-                    tmem_ld32(tmem + lane_off + kTmY + 32 * half, yv);
+                    tmem_ld32(tmem + lane_off + kTmY + 32 * hn, yv);
                     tmem_ld_wait();
 #pragma unroll
                     for (int cc = 0; cc < 4; ++cc) {
@@ -583,32 +625,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ow[e] = pack_bf2(yv[8 * cc + 2 * e], yv[8 * cc + 2 * e + 1]);
                             bad |= bf2_nonfinite(ow[e]);
                         }
-                        *reinterpret_cast<uint4 *>(ybuf + swz(lane, 4 * half + cc)) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+                        *reinterpret_cast<uint4 *>(ybuf + swz(lane, 4 * hn + cc)) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
                     }
                 }
                 fence_async_smem();
                 tc_fence_before();
-                __syncwarp();
+                pair_sync(q);
                 if (lane == 0) {
-                    if (c * kBlk + 32 * q < p.T) {
+                    if (hn == 0 && c * kBlk + 32 * q < p.T) {
                         tma_store_3d(&tm_y, ybuf_a, h * kP, c * kBlk + 32 * q, bi);
                         bulk_commit();
                     }
                     mbar_arrive(bar(B_EMPTY + st));
                 }
             }
-            // the final state (state rows): h after the last block's product, which (5) waited for
+            // the final state (state rows, this warp's half of p): h after the last block's
+            // product, which (5) waited for
             if (q < 2 && p.final_state) {
+                float hv[32];
+                tmem_ld32(tmem + lane_off + kTmH + 32 * hn, hv);
+                tmem_ld_wait();
+                float *dst = p.final_state + ((int64_t)sq * kN + i) * kP + 32 * hn;
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    float hv[32];
-                    tmem_ld32(tmem + lane_off + kTmH + 32 * half, hv);
-                    tmem_ld_wait();
-                    float *dst = p.final_state + ((int64_t)sq * kN + i) * kP + 32 * half;
-#pragma unroll
-                    for (int e = 0; e < 32; e += 4)
-                        *reinterpret_cast<float4 *>(dst + e) = make_float4(hv[e], hv[e + 1], hv[e + 2], hv[e + 3]);
-                }
+                for (int e = 0; e < 32; e += 4)
+                    *reinterpret_cast<float4 *>(dst + e) = make_float4(hv[e], hv[e + 1], hv[e + 2], hv[e + 3]);
             }
         }
         if (lane == 0) bulk_wait0();
