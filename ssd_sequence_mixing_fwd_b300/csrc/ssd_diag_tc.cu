@@ -77,9 +77,9 @@ constexpr int kTabRow = 36;                            // floats per table row (
 constexpr int kTabRows = 20;                           // per warp: T2 T3 g x 2 groups, G x 2 groups x 7
 constexpr int kTabWarpBytes = kTabRows * kTabRow * 4;
 constexpr int kOffTab = kOffY + kTile;                 // per math warp: tables of its n half
-constexpr int kDpRow = 20;                             // floats per row of the partial sums (16 + padding)
-constexpr int kOffDp = kOffTab + kMathWarps * kTabWarpBytes;   // [128][kDpRow] partial diagonal-group sums
-constexpr int kOffDtW = kOffDp + 128 * kDpRow * 4;     // per math warp: Dt of all 128 rows
+// The partial diagonal-group sums of the two warps of a quarter ([2][32 rows][16]) share the
+// quarter's y buffer: they are read before the buffer takes y.
+constexpr int kOffDtW = kOffTab + kMathWarps * kTabWarpBytes;   // per math warp: Dt of all 128 rows
 constexpr int kOffA2 = kOffDtW + kMathWarps * 512;     // per math warp: A (log2 units) of its n half
 constexpr int kOffMisc = kOffA2 + kMathWarps * 128;    // TMEM base, abort flag
 constexpr int kOffBar = kOffMisc + 16;
@@ -274,7 +274,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         float *DtW = reinterpret_cast<float *>(smem + kOffDtW + (warp - 2) * 512);
         float *A2h = reinterpret_cast<float *>(smem + kOffA2 + (warp - 2) * 128);
         float *Bp = reinterpret_cast<float *>(smem + kOffBp);
-        float *Dp = reinterpret_cast<float *>(smem + kOffDp) + i * kDpRow;
+        // partial sums of half hh for this row; 16-byte chunk k at k ^ ((lane >> 1) & 3), so the
+        // 64-byte rows of eight consecutive lanes cover all banks
+        auto dpart = [&](int hh, int k) {
+            return reinterpret_cast<float4 *>(smem + kOffY + q * 4096 + hh * 2048 + lane * 64) + (k ^ ((lane >> 1) & 3));
+        };
         unsigned char *ybuf = smem + kOffY + q * 4096;
         const uint32_t ybuf_a = sbase + kOffY + q * 4096;
         // Per-warp tables over this warp's half of n, each factor in (0, 1]:
@@ -532,9 +536,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) mbar_arrive(bar(B_OPS));
 
                 // (4) the diagonal group over this warp's half of n: S_ij = sum_n C~_in B'_jn,
-                // j <= i (fp32; while the MMAs run), two rows j at a time.  The B' rows of the
-                // group were written by this warp and its partner: the pair barrier below orders
-                // them (and the partner's partial sums) before their use.
+                // j <= i (fp32; while the MMAs run).  The B' rows of the group were written by this
+                // warp and its partner: the pair barrier orders them before their use (and the
+                // quarter's previous y store has read the buffer the partial sums go to).
+                if (hn == 0 && lane == 0) bulk_wait_read0();
                 pair_sync(q);
                 float d[16];
                 if (safe) {
@@ -560,30 +565,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int jj = 0; jj < 16; ++jj) d[jj] = dl[jj];
                 }
-                // the partner that does not merge the diagonal group hands over its partial sums;
-                // the y store of the previous block has read the quarter's buffer by the same barrier
-                if (!need_d) {
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        *reinterpret_cast<float4 *>(Dp + 4 * k) = make_float4(d[4 * k], d[4 * k + 1], d[4 * k + 2], d[4 * k + 3]);
-                }
-                if (hn == 0 && lane == 0) bulk_wait_read0();
+                for (int k = 0; k < 4; ++k) *dpart(hn, k) = make_float4(d[4 * k], d[4 * k + 1], d[4 * k + 2], d[4 * k + 3]);
                 pair_sync(q);
-                if (need_d) {
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const float4 o = *reinterpret_cast<const float4 *>(Dp + 4 * k);
-                        d[4 * k] += o.x;
-                        d[4 * k + 1] += o.y;
-                        d[4 * k + 2] += o.z;
-                        d[4 * k + 3] += o.w;
-                    }
-                }
 
                 // (5) S: the copies' products left of the diagonal group, the diagonal group,
                 // zeros right of it -> fp16 (this warp: S columns 64 hn .. 64 hn + 63)
                 wait_bar(ctl, bar(B_SFULL), kb & 1);
                 tc_fence_after();
+                float dsum[16];
+                if (need_d) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float4 a = *dpart(0, k), b = *dpart(1, k);
+                        dsum[4 * k] = a.x + b.x;
+                        dsum[4 * k + 1] = a.y + b.y;
+                        dsum[4 * k + 2] = a.z + b.z;
+                        dsum[4 * k + 3] = a.w + b.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) dsum[k] = 0.f;
+                }
 #pragma unroll 1
                 for (int k2 = 0; k2 < 2; ++k2) {
                     float sv[32];
@@ -597,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int u = 0; u < 2; ++u) {
                             const int col = 32 * k2 + 2 * e + u;          // within this warp's 64 columns
                             const int Jg = 4 * hn + (col >> 4);
-                            v2[u] = Jg < I ? sv[2 * e + u] : (Jg == I ? d[col & 15] : 0.f);
+                            v2[u] = Jg < I ? sv[2 * e + u] : (Jg == I ? dsum[col & 15] : 0.f);
                         }
                         w[e] = pack_h2(v2[0], v2[1]);
                     }
@@ -613,6 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // buffer -> TMA store
                 wait_bar(ctl, bar(B_YFULL), kb & 1);
                 tc_fence_after();
+                pair_sync(q);   // the partial sums in the y buffer have been read
                 {
                     float yv[32];
                     tmem_ld32(tmem + lane_off + kTmY + 32 * hn, yv);
