@@ -35,7 +35,7 @@
 // rounding); the block of 128 tokens plays the chunk's part whatever Q is.
 //
 // One CTA per (batch row, head) at a time (persistent over sequences), 10 warps:
-//   warp 0      TMA producer: X, B, C tiles of a block (two stages)
+//   warp 0      producer: X, B, C tiles of a block by TMA, its dt by plain loads (two stages)
 //   warp 1      TMEM owner; lane 0 issues every MMA
 //   warps 2-9   math, two per TMEM lane quarter: thread = TMEM lane = row i of the
 //               block (warp w owns lanes 32 (w mod 4) ...), the two warps of a quarter
@@ -81,7 +81,8 @@ constexpr int kOffTab = kOffY + kTile;                 // per math warp: tables 
 // quarter's y buffer: they are read before the buffer takes y.
 constexpr int kOffDtW = kOffTab + kMathWarps * kTabWarpBytes;   // per math warp: Dt of all 128 rows
 constexpr int kOffA2 = kOffDtW + kMathWarps * 512;     // per math warp: A (log2 units) of its n half
-constexpr int kOffMisc = kOffA2 + kMathWarps * 128;    // TMEM base, abort flag
+constexpr int kOffDt = kOffA2 + kMathWarps * 128;      // [2 stages][128] dt of the stage's block
+constexpr int kOffMisc = kOffDt + 2 * 512;             // TMEM base, abort flag
 constexpr int kOffBar = kOffMisc + 16;
 constexpr int kNumBars = 8;
 constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 1024;   // + alignment slack
@@ -194,15 +195,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int hpg = p.H / p.G;
 
     if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            int kb = 0;
-            bool ok = true;
-            for (int sq = blockIdx.x; sq < p.nseq && ok; sq += gridDim.x) {
-                const int bi = sq / p.H, h = sq - bi * p.H, g = h / hpg;
-                for (int c = 0; c < p.nblk; ++c, ++kb) {
-                    const int st = kb & 1;
-                    if (kb >= 2 && !(ok = wait_bar(ctl, bar(B_EMPTY + st), ((kb >> 1) - 1) & 1))) break;
+        // ------------------------------------------------------------ producer
+        // The whole warp loads the block's dt (one strided word per token) into the stage; lane 0
+        // then arms the stage's barrier (its arrival releases those stores) and issues the TMA.
+        int kb = 0;
+        bool ok = true;
+        for (int sq = blockIdx.x; sq < p.nseq && ok; sq += gridDim.x) {
+            const int bi = sq / p.H, h = sq - bi * p.H, g = h / hpg;
+            for (int c = 0; c < p.nblk; ++c, ++kb) {
+                const int st = kb & 1;
+                if (kb >= 2 && !(ok = __all_sync(0xffffffffu, wait_bar(ctl, bar(B_EMPTY + st), ((kb >> 1) - 1) & 1))))
+                    break;
+                float *dts = reinterpret_cast<float *>(smem + kOffDt + st * 512);
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const int t = c * kBlk + 32 * m + lane;
+                    dts[32 * m + lane] = t < p.T ? __ldg(p.dt + ((int64_t)bi * p.T + t) * p.H + h) : 0.f;
+                }
+                __syncwarp();
+                if (lane == 0) {
                     const uint32_t dst = sbase + kOffStage + st * kStageBytes;
                     mbar_expect_tx(bar(B_FULL + st), 3 * kTile);
                     tma_load_3d(dst, &tm_x, bar(B_FULL + st), h * kP, c * kBlk, bi);
@@ -210,11 +221,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_3d(dst + 2 * kTile, &tm_C, bar(B_FULL + st), g * kN, c * kBlk, bi);
                 }
             }
-            // after an abort: wait (bounded) for the loads still in flight
-            if (!ok)
-                for (int k2 = kb - 2; k2 < kb; ++k2)
-                    if (k2 >= 0) drain_bar(bar(B_FULL + (k2 & 1)), (k2 >> 1) & 1);
         }
+        // after an abort: wait (bounded) for the loads still in flight
+        if (!ok && lane == 0)
+            for (int k2 = kb - 2; k2 < kb; ++k2)
+                if (k2 >= 0) drain_bar(bar(B_FULL + (k2 & 1)), (k2 >> 1) & 1);
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
@@ -326,15 +337,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_st32(tmem + lane_off + kTmH + 32 * hn, v);
                 tmem_st_wait();
             }
-            auto load_dt = [&](int c, float (&v)[4]) {
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const int t = c * kBlk + 32 * m + lane;
-                    v[m] = t < p.T ? __ldg(p.dt + ((int64_t)bi * p.T + t) * p.H + h) : 0.f;
-                }
-            };
-            float dtn[4];
-            load_dt(0, dtn);
             // (1) + (2) of a block, run for block c + 1 while block c's S X is in flight:
             // Dt, the inclusive prefix sums of dt over the block (four interleaved 32-row scans;
             // every warp computes all 128 rows), the warp's tables, and the state rows' h_prev
@@ -343,11 +345,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             // h_prev tile, have completed)
             float Dti = 0.f, Dend = 0.f, RI = 0.f, Rm1 = 0.f;
             bool safe = true;
-            auto prep = [&](int c) {
+            // (the stage of block kb2 has landed: its dt, and the tiles used later)
+            auto prep = [&](int kb2) {
+                const int st2 = kb2 & 1;
+                wait_bar(ctl, bar(B_FULL + st2), (kb2 >> 1) & 1);
+                const float *dts = reinterpret_cast<const float *>(smem + kOffDt + st2 * 512);
                 float Dv[4];
 #pragma unroll
-                for (int m = 0; m < 4; ++m) Dv[m] = dtn[m];
-                if (c + 1 < p.nblk) load_dt(c + 1, dtn);
+                for (int m = 0; m < 4; ++m) Dv[m] = dts[32 * m + lane];
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
 #pragma unroll
@@ -408,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_st32(tmem + lane_off + kTmH + 32 * hn, hv);
                 }
             };
-            prep(0);
+            prep(kb);
             for (int c = 0; c < p.nblk; ++c, ++kb) {
                 const int st = kb & 1;
 
@@ -610,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(B_S16));
-                if (c + 1 < p.nblk) prep(c + 1);
+                if (c + 1 < p.nblk) prep(kb + 1);
 
                 // (6) epilogue: y = Y (bf16; this warp: columns 32 hn ..) -> the quarter's 32-row
                 // buffer -> TMA store
