@@ -87,11 +87,13 @@ extern "C" {
  * b == 0 or T == 0 is a valid empty problem: y is empty and final_state is
  * init_state (or zero).  A ragged last chunk (T % Q != 0) is allowed.
  * Domain (not checked on the device): dt >= 0 and A <= 0, all finite.  The
- * fused path keeps its matrix operands in fp16: when x, B, C, a C B^T entry
+ * tcgen05 paths keep their matrix operands in fp16: when x, B, C, a C B^T entry
  * or a state entry entering a 128-token block leaves the fp16 range
  * (|v| > 65504), the call reports SSD_ERR_DEVICE through
  * ssd_check_device_status and its outputs are invalid; the generic path has
- * no such limit (SSD_PATH_GENERIC computes such inputs in fp32). */
+ * no such limit (SSD_PATH_GENERIC computes such inputs in fp32).  Outside the
+ * domain (a growing decay) the tcgen05 paths' decay factors can leave fp16 as
+ * well, with the same report. */
 typedef struct ssd_dims {
     int64_t b, T, H, P, N, G, Q;
     int32_t a_mode;    /* SSD_A_SCALAR or SSD_A_DIAGONAL                       */
@@ -100,13 +102,18 @@ typedef struct ssd_dims {
     int32_t reserved;  /* must be 0                                            */
 } ssd_dims;
 
-/* Paths.  SSD_PATH_TCGEN05 (one fused persistent kernel: TMA loads, tcgen05
- * tensor-core products with TMEM accumulators, block-to-block state hand-off
- * through an L2-resident ring) takes scalar A, bf16 io, P == 64, N in
- * {128, 256} and Q in {128, 256}; it evaluates every chunk as 128-token blocks
- * (for Q = 256, two blocks per chunk -- the chunked algorithm applied inside
- * the chunk, equal up to rounding).  SSD_PATH_GENERIC (fp32 CUDA-core kernels) takes
- * every dims the ABI accepts.  SSD_PATH_AUTO picks TCGEN05 where it applies.
+/* Paths.  SSD_PATH_TCGEN05 is one persistent kernel with TMA loads and tcgen05
+ * tensor-core products accumulating in TMEM:
+ *  - scalar A: bf16 io, P == 64, N in {128, 256}, Q in {128, 256}; the state
+ *    passes block to block through an L2-resident ring;
+ *  - diagonal A: bf16 io, P == N == 64, any Q; one CTA per (batch row, head) at
+ *    a time keeps the state in TMEM, and every decay is split at a reference
+ *    token so that the fp16 operands carry factors <= 1 (the pairs inside one
+ *    16-token group are summed in fp32 on the CUDA cores).
+ * Both evaluate every chunk as 128-token blocks (the chunked algorithm applied
+ * inside the chunk, equal up to rounding).  SSD_PATH_GENERIC (fp32 CUDA-core
+ * kernels) takes every dims the ABI accepts.  SSD_PATH_AUTO picks TCGEN05 where
+ * it applies.
  *
  * Bytes of device workspace ssd_fwd needs for `dims` (written to *bytes).
  * Host-only; enqueues nothing.  Returns SSD_ERR_INVALID_ARG /
