@@ -13,6 +13,9 @@ Two independent evaluations of the same map live here:
 * :mod:`oracle.brute` -- numpy fp64: the materialised lower-triangular matrix
   M of the same page and section, and the masked-attention form of the
   scalar case.  It pins the recurrence on tiny inputs.
+* :func:`recurrence_bwd` -- the C library's reverse mode of the same
+  recurrence (the gradients of sum y*dy + sum final_state*dfinal), pinned by
+  central finite differences of the dense form of :mod:`oracle.brute`.
 """
 import ctypes
 import os
@@ -41,6 +44,10 @@ def _load():
                 + [ctypes.c_void_p] * 7
                 + [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64]
                 + [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int])
+            lib.ssd_oracle_bwd.restype = ctypes.c_int
+            lib.ssd_oracle_bwd.argtypes = (
+                [ctypes.c_int64] * 6 + [ctypes.c_int]
+                + [ctypes.c_void_p] * 16 + [ctypes.c_int, ctypes.c_int])
             lib.ssd_oracle_threads.restype = ctypes.c_int
             lib.ssd_oracle_threads.argtypes = [ctypes.c_int]
             _lib = lib
@@ -112,3 +119,40 @@ def recurrence(x, dt, A, B, C, D=None, init_state=None, streams=None, t_end=None
         y = y.reshape(nb, H, t_end, P).transpose(0, 2, 1, 3).copy()
         fin = fin.reshape(nb, H, N, P)
     return y, fin
+
+
+def _f64(a):
+    if a is None:
+        return None
+    if hasattr(a, "detach"):
+        a = a.detach().cpu().double().numpy()
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def recurrence_bwd(x, dt, A, B, C, D=None, init_state=None, dy=None, dfinal=None, nthreads=None, plant=0):
+    """fp64 gradients of L = sum y*dy + sum final_state*dfinal (the reverse mode of the recurrence).
+
+    Inputs as for :func:`recurrence` (whole tensors), ``dy`` (b,T,H,P) and ``dfinal``
+    (b,H,N,P) or None.  Returns a dict with dx, ddt, dA, dB, dC, dD (None without D) and
+    dinit, fp64, in the layouts of the corresponding inputs.
+    """
+    x, dt, A, B, C = (_f32(v) for v in (x, dt, A, B, C))
+    D, init_state = _f32(D), _f32(init_state)
+    dy, dfinal = _f64(dy), _f64(dfinal)
+    nb, T, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    a_mode = A_SCALAR if A.ndim == 1 else A_DIAGONAL
+    assert dy is not None and dy.shape == x.shape
+    if dfinal is not None:
+        assert dfinal.shape == (nb, H, N, P)
+    out = dict(dx=np.zeros((nb, T, H, P)), ddt=np.zeros((nb, T, H)), dA=np.zeros(A.shape),
+               dB=np.zeros((nb, T, G, N)), dC=np.zeros((nb, T, G, N)),
+               dD=np.zeros((H,)) if D is not None else None, dinit=np.zeros((nb, H, N, P)))
+    rc = _load().ssd_oracle_bwd(
+        nb, T, H, P, N, G, a_mode,
+        _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(init_state), _ptr(dy), _ptr(dfinal),
+        _ptr(out["dx"]), _ptr(out["ddt"]), _ptr(out["dA"]), _ptr(out["dB"]), _ptr(out["dC"]),
+        _ptr(out["dD"]), _ptr(out["dinit"]), int(nthreads or 0), int(plant))
+    if rc != 0:
+        raise ValueError("ssd_oracle_bwd rejected its arguments (status %d)" % rc)
+    return out
