@@ -204,6 +204,40 @@ SSD_API int ssd_decode_step(const ssd_dims *dims,
             float *state, void *y,
             void *stream);
 
+/* Backward pass: the gradients of
+ *   L = sum y * dy + sum final_state * dfinal
+ * for the map ssd_fwd computes (the chunked algorithm's training cost is
+ * what Structured State Space Duality, "The chunked algorithm takes both",
+ * weighs; the pages give no backward, so this is the chain rule of the
+ * recurrence of "The recurrence as one matrix").  CUDA cores, fp32
+ * arithmetic: a forward sweep stores the state at the start of every
+ * 32-token block, and a reverse sweep recomputes each block's states from it
+ * while it runs the adjoint recurrence g = C_t dy_t^T + a_{t+1} (.) g.
+ *
+ * Inputs (device memory, layouts of ssd_fwd): x, dt, A, B, C, D (or NULL),
+ * init_state (or NULL) as given to the forward call; dy (b,T,H,P) io dtype;
+ * dfinal (b,H,N,P) float32 or NULL (zero).  Outputs, all written (none
+ * accumulated into):
+ *   dx (b,T,H,P) io dtype      ddt (b,T,H) float32    dA like A, float32
+ *   dB, dC (b,T,G,N) io dtype (summed over the heads of each group)
+ *   dD (H) float32 or NULL (not computed; sum of dy . x per head)
+ *   dinit (b,H,N,P) float32 or NULL (not computed)
+ * dims->path must be SSD_PATH_AUTO or SSD_PATH_GENERIC (SSD_ERR_UNSUPPORTED
+ * otherwise); the backward takes 4 <= P <= 128.  Every pointer 16-byte
+ * aligned; workspace >= ssd_bwd_workspace_size bytes, 256-byte aligned
+ * (checkpoints b*H*ceil(N/(1024/P))*ceil(T/32)*4 KB plus fp32 per-token
+ * arrays of 3*b*T*H*N + b*T*H*P floats).  Asynchronous on `stream`; on any
+ * argument error nothing is enqueued.  b == 0 or T == 0: dA and dD are zero
+ * and dinit is dfinal (or zero). */
+SSD_API int ssd_bwd_workspace_size(const ssd_dims *dims, size_t *bytes);
+SSD_API int ssd_bwd(const ssd_dims *dims,
+            const void *x, const float *dt, const float *A,
+            const void *B, const void *C, const float *D,
+            const float *init_state, const void *dy, const float *dfinal,
+            void *dx, float *ddt, float *dA, void *dB, void *dC,
+            float *dD, float *dinit,
+            void *workspace, size_t workspace_bytes, void *stream);
+
 /* Allocation-free forward pass.  The paper has no counterpart to this entry
  * point; it exists for callers that may not allocate device memory
  * themselves: for example a plug-in inside a host application that owns the

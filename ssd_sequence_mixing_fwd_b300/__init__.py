@@ -43,7 +43,7 @@ _PATHS = {"auto": SSD_PATH_AUTO, "generic": SSD_PATH_GENERIC, "tcgen05": SSD_PAT
 EXPORTED = ("ssd_fwd_workspace_size", "ssd_fwd_path", "ssd_fwd", "ssd_check_device_status",
             "ssd_status_string", "ssd_abi_version", "ssd_debug_set_wait",
             "ssd_debug_set_kernel_events", "ssd_launch_count", "ssd_fwd_noalloc", "ssd_last_cuda_error",
-            "ssd_scan", "ssd_decode_step")
+            "ssd_scan", "ssd_decode_step", "ssd_bwd_workspace_size", "ssd_bwd")
 
 
 class ssd_dims(ctypes.Structure):
@@ -82,6 +82,8 @@ def load_library(path=LIB_PATH):
             lib.ssd_fwd_noalloc.argtypes = [P_dims] + [vp] * 9 + [vp]
             lib.ssd_scan.argtypes = [P_dims] + [vp] * 9 + [vp]
             lib.ssd_decode_step.argtypes = [P_dims] + [vp] * 8 + [vp]
+            lib.ssd_bwd_workspace_size.argtypes = [P_dims, ctypes.POINTER(sz)]
+            lib.ssd_bwd.argtypes = [P_dims] + [vp] * 16 + [vp, sz, vp]
             lib.ssd_check_device_status.argtypes = [vp, sz, vp]
             lib.ssd_status_string.argtypes = [ctypes.c_int]
             lib.ssd_status_string.restype = ctypes.c_char_p
@@ -94,7 +96,7 @@ def load_library(path=LIB_PATH):
             for name in ("ssd_fwd_workspace_size", "ssd_fwd_path", "ssd_fwd",
                          "ssd_check_device_status", "ssd_abi_version", "ssd_debug_set_wait",
                          "ssd_debug_set_kernel_events", "ssd_launch_count", "ssd_fwd_noalloc",
-                         "ssd_scan", "ssd_decode_step"):
+                         "ssd_scan", "ssd_decode_step", "ssd_bwd_workspace_size", "ssd_bwd"):
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -268,6 +270,49 @@ def ssd_decode_step(x, dt, A, B, C, D, state, y=None, stream=None):
     if st != SSD_OK:
         raise SSDError(st, "ssd_decode_step")
     return y
+
+
+def ssd_bwd_workspace_size(dims):
+    n = ctypes.c_size_t(0)
+    st = load_library().ssd_bwd_workspace_size(ctypes.byref(dims), ctypes.byref(n))
+    if st != SSD_OK:
+        raise SSDError(st, "ssd_bwd_workspace_size")
+    return n.value
+
+
+def ssd_bwd(x, dt, A, B, C, D=None, init_state=None, dy=None, dfinal=None, want_dD=True, want_dinit=True,
+            workspace=None, stream=None):
+    """Gradients of ``sum y*dy + sum final_state*dfinal`` for the map :func:`ssd_fwd` computes.
+
+    Returns a dict with dx (like x), ddt (b,T,H) fp32, dA (like A) fp32, dB and dC (like B) in
+    the io dtype, dD (H) fp32 (None unless ``want_dD``) and dinit (b,H,N,P) fp32 (None unless
+    ``want_dinit``).  ``dy`` has x's shape and dtype; ``dfinal`` is (b,H,N,P) fp32 or None.
+    Asynchronous on the current stream."""
+    import torch
+    if dy is None or dy.shape != x.shape or dy.dtype != x.dtype or not dy.is_cuda or not dy.is_contiguous():
+        raise ValueError("dy must be a contiguous CUDA tensor with x's shape and dtype")
+    if dfinal is not None and (dfinal.dtype != torch.float32 or not dfinal.is_cuda or not dfinal.is_contiguous()):
+        raise ValueError("dfinal must be a contiguous float32 CUDA tensor")
+    dims, args, _, _, _, s = _marshal(x, dt, A, B, C, D, init_state, 256, False, "auto", x, None,
+                                      _NO_WORKSPACE, stream)
+    b, T, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    if dfinal is not None and tuple(dfinal.shape) != (b, H, N, P):
+        raise ValueError("dfinal must be (b,H,N,P)")
+    dev = x.device
+    out = dict(dx=torch.empty_like(x), ddt=torch.empty_like(dt), dA=torch.empty_like(A),
+               dB=torch.empty_like(B), dC=torch.empty_like(C),
+               dD=torch.empty((H,), device=dev, dtype=torch.float32) if want_dD else None,
+               dinit=torch.empty((b, H, N, P), device=dev, dtype=torch.float32) if want_dinit else None)
+    if workspace is None:
+        workspace = torch.empty(max(ssd_bwd_workspace_size(dims), 256), device=dev, dtype=torch.uint8)
+    st = load_library().ssd_bwd(args[0], *args[1:8], _ptr(dy), _ptr(dfinal), _ptr(out["dx"]), _ptr(out["ddt"]),
+                                _ptr(out["dA"]), _ptr(out["dB"]), _ptr(out["dC"]), _ptr(out["dD"]),
+                                _ptr(out["dinit"]), _ptr(workspace), workspace.numel(),
+                                ctypes.c_void_p(s.cuda_stream))
+    if st != SSD_OK:
+        raise SSDError(st, "ssd_bwd")
+    return out
 
 
 class PreparedCall:

@@ -174,6 +174,57 @@ extern "C" int ssd_fwd(const ssd_dims *dims, const void *x, const float *dt, con
     return note_cuda(e);
 }
 
+// Backward: the gradients of sum y * dy + sum final_state * dfinal (CUDA cores).
+static int bwd_check(const ssd_dims *dims, Problem *p) {
+    int st = check_dims(dims, p);
+    if (st != SSD_OK) return st;
+    if (dims->path == SSD_PATH_TCGEN05) return SSD_ERR_UNSUPPORTED;
+    return bwd_supports(*p) ? SSD_OK : SSD_ERR_UNSUPPORTED;
+}
+
+extern "C" int ssd_bwd_workspace_size(const ssd_dims *dims, size_t *bytes) {
+    if (!bytes) return SSD_ERR_INVALID_ARG;
+    Problem p;
+    const int st = bwd_check(dims, &p);
+    if (st != SSD_OK) return st;
+    *bytes = bwd_workspace_bytes(p);
+    return SSD_OK;
+}
+
+extern "C" int ssd_bwd(const ssd_dims *dims, const void *x, const float *dt, const float *A, const void *B,
+                       const void *C, const float *D, const float *init_state, const void *dy,
+                       const float *dfinal, void *dx, float *ddt, float *dA, void *dB, void *dC, float *dD,
+                       float *dinit, void *workspace, size_t workspace_bytes, void *stream) {
+    Problem p;
+    int st = bwd_check(dims, &p);
+    if (st != SSD_OK) return st;
+    const bool empty = (p.b == 0 || p.T == 0);
+    if (!A || (!empty && (!x || !dt || !B || !C || !dy || !dx || !ddt || !dB || !dC)) || !dA)
+        return SSD_ERR_INVALID_ARG;
+    const void *ptrs[] = {x, dt, A, B, C, D, init_state, dy, dfinal, dx, ddt, dA, dB, dC, dD, dinit};
+    for (const void *q : ptrs)
+        if (q && !aligned16(q)) return SSD_ERR_ALIGNMENT;
+    const size_t need = bwd_workspace_bytes(p);
+    if (!workspace || workspace_bytes < need) return SSD_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SSD_ERR_ALIGNMENT;
+    p.x = x; p.dt = dt; p.A = A; p.B = B; p.C = C; p.D = D; p.init = init_state;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t nA = sizeof(float) * (size_t)(p.a_mode == SSD_A_SCALAR ? p.H : p.H * p.N);
+    cudaError_t e;
+    if (empty) {
+        // no token: dA = dD = 0 and the initial state's gradient is dfinal itself
+        const size_t ns = sizeof(float) * (size_t)(p.b * p.H * p.N * p.P);
+        e = cudaMemsetAsync(workspace, 0, kStatusBytes, s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(dA, 0, nA, s);
+        if (e == cudaSuccess && dD) e = cudaMemsetAsync(dD, 0, sizeof(float) * (size_t)p.H, s);
+        if (e == cudaSuccess && dinit && ns)
+            e = dfinal ? cudaMemcpyAsync(dinit, dfinal, ns, cudaMemcpyDeviceToDevice, s) : cudaMemsetAsync(dinit, 0, ns, s);
+        return note_cuda(e);
+    }
+    BwdGrads g{dy, dfinal, dx, ddt, dA, dB, dC, dD, dinit};
+    return note_cuda(bwd_launch(p, g, workspace, s));
+}
+
 // The linear form (ssd_scan) and its one-token case (ssd_decode_step): same argument checks as
 // ssd_fwd, no workspace.
 static int scan_call(const ssd_dims *dims, const void *x, const float *dt, const float *A, const void *B,

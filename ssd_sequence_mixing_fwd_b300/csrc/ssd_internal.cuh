@@ -56,6 +56,21 @@ bool diag_supports(const Problem &p);
 size_t diag_workspace_bytes(const Problem &p);
 cudaError_t diag_launch(const Problem &p, void *ws, cudaStream_t s);
 
+// ---- backward (csrc/ssd_bwd.cu): gradient buffers of one call
+struct BwdGrads {
+    const void *dy;        // (b,T,H,P) io dtype
+    const float *dfinal;   // (b,H,N,P) or null
+    void *dx;              // (b,T,H,P) io dtype
+    float *ddt;            // (b,T,H)
+    float *dA;             // like A
+    void *dB, *dC;         // (b,T,G,N) io dtype
+    float *dD;             // (H) or null
+    float *dinit;          // (b,H,N,P) or null
+};
+bool bwd_supports(const Problem &p);
+size_t bwd_workspace_bytes(const Problem &p);
+cudaError_t bwd_launch(const Problem &p, const BwdGrads &g, void *ws, cudaStream_t s);
+
 // ---- linear-form scan (csrc/ssd_scan.cu): no workspace ---------------------
 bool scan_supports(const Problem &p);
 cudaError_t scan_launch(const Problem &p, cudaStream_t s);

@@ -175,3 +175,23 @@ def test_scan_and_decode_reject_bad_arguments_before_any_launch(lib):
     a[1] = ctypes.c_void_p((1 << 21) + 4096 + 2)         # dt not 4-byte aligned
     assert lib.ssd_scan(ctypes.byref(dims()), *a, None) == ssd.SSD_ERR_ALIGNMENT
     assert lib.ssd_scan(ctypes.byref(dims(Q=96)), *args, None) == ssd.SSD_ERR_INVALID_ARG
+
+
+def test_backward_argument_checks_enqueue_nothing(lib):
+    # every refusal happens before any CUDA call, so fake device addresses are safe here
+    vp = lambda i: ctypes.c_void_p((1 << 21) + 4096 * i)
+    args = [vp(i) for i in range(16)]
+    d = dims(path="auto")
+    ws_ok = (vp(40), 1 << 40)
+    bad = list(args)
+    bad[7] = None                                                    # dy missing
+    assert lib.ssd_bwd(ctypes.byref(d), *bad, *ws_ok, None) == ssd.SSD_ERR_INVALID_ARG
+    bad = list(args)
+    bad[0] = ctypes.c_void_p((1 << 21) + 8)                          # x not 16-byte aligned
+    assert lib.ssd_bwd(ctypes.byref(d), *bad, *ws_ok, None) == ssd.SSD_ERR_ALIGNMENT
+    assert lib.ssd_bwd(ctypes.byref(d), *args, vp(40), 256, None) == ssd.SSD_ERR_WORKSPACE
+    d2 = dims(path="tcgen05")
+    assert lib.ssd_bwd(ctypes.byref(d2), *args, *ws_ok, None) == ssd.SSD_ERR_UNSUPPORTED
+    d3 = dims(P=256, N=64)
+    n = ctypes.c_size_t(0)
+    assert lib.ssd_bwd_workspace_size(ctypes.byref(d3), ctypes.byref(n)) == ssd.SSD_ERR_UNSUPPORTED

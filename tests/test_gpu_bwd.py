@@ -1,0 +1,112 @@
+"""GPU parity of the backward pass (``ssd_bwd``, through the C ABI) against the fp64 backward oracle.
+
+Every gradient -- dx, ddt, dA, dB, dC, dD, dinit -- is compared on the whole
+tensor (relative L2).  Tolerances: fp32 io 1e-5 (fp32 arithmetic throughout);
+bf16 io 2e-3 (dx, dB and dC are rounded to bf16 on output; the fp32 outputs
+ddt, dA, dD and dinit are held to 1e-4).  Cases cover both A modes, D and the
+initial state present or absent, dfinal present or absent, several B/C
+groups, ragged lengths around the 32-token checkpoint block, a state
+dimension that does not fill its last slice of rows, and the head dims the
+kernel takes.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import ssd_sequence_mixing_fwd_b300 as ssd
+from ssd_sequence_mixing_fwd_b300.inputs import Workload, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def rel(a, b):
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    nb = np.linalg.norm(b)
+    return float(np.linalg.norm(a - b) / nb) if nb > 0 else float(np.linalg.norm(a))
+
+
+def cotangents(w, seed, with_dfinal):
+    g = torch.Generator().manual_seed(seed)
+    io = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    dy = torch.randn((w.b, w.T, w.H, w.P), generator=g).to(io)
+    df = torch.randn((w.b, w.H, w.N, w.P), generator=g) if with_dfinal else None
+    return dy, df
+
+
+def run_and_check(w, seed=0, with_dfinal=True, drop_D=False, dt_scale=1.0, device="cuda:0"):
+    inp = make_inputs(w)
+    inp["dt"] = inp["dt"] * dt_scale
+    if drop_D:
+        inp["D"] = None
+    dy, df = cotangents(w, 100 + seed, with_dfinal)
+    d = {k: (None if v is None else v.to(device)) for k, v in inp.items()}
+    got = ssd.ssd_bwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["init_state"], dy.to(device),
+                      None if df is None else df.to(device), want_dD=inp["D"] is not None)
+    torch.cuda.synchronize()
+    ref = oracle.recurrence_bwd(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"], inp["init_state"],
+                                dy.double().numpy(), None if df is None else df.double().numpy())
+    io_tol = 2e-3 if w.dtype == "bf16" else 1e-5
+    f32_tol = 1e-4 if w.dtype == "bf16" else 1e-5
+    errs = {}
+    for k, tol in (("dx", io_tol), ("dB", io_tol), ("dC", io_tol), ("ddt", f32_tol), ("dA", f32_tol),
+                   ("dD", f32_tol), ("dinit", f32_tol)):
+        if ref[k] is None:
+            continue
+        g = got[k].float().cpu().numpy()
+        assert np.isfinite(g).all(), k
+        errs[k] = rel(g, ref[k])
+        assert errs[k] <= tol, "%s relL2 %.3g > %.3g" % (k, errs[k], tol)
+    return errs
+
+
+CASES = [
+    ("scalar_bf16", Workload("t", b=2, T=100, H=4, P=64, N=128, G=2, Q=128, D="normal", init_std=0.1, seed=701)),
+    ("diag_bf16", Workload("t", b=2, T=77, H=4, P=64, N=64, G=1, Q=64, a_mode="diagonal", D="none",
+                           init_std=0.2, seed=702)),
+    ("scalar_f32", Workload("t", b=1, T=130, H=3, P=16, N=16, G=1, Q=64, dtype="f32", D="ones", seed=703)),
+    ("diag_f32_N50", Workload("t", b=2, T=65, H=2, P=32, N=50, G=2, Q=128, dtype="f32", a_mode="diagonal",
+                              D="normal", init_std=0.3, seed=704)),
+    ("scalar_bf16_P128_N128", Workload("t", b=1, T=40, H=2, P=128, N=128, G=1, Q=128, D="normal", seed=705)),
+    ("scalar_f32_P4_T1", Workload("t", b=3, T=1, H=2, P=4, N=8, G=1, Q=64, dtype="f32", D="normal",
+                                  init_std=0.5, seed=706)),
+    ("scalar_bf16_T32", Workload("t", b=1, T=32, H=2, P=64, N=128, G=1, Q=128, D="none", seed=707)),
+]
+
+
+@pytest.mark.parametrize("name,w", CASES, ids=[c[0] for c in CASES])
+def test_backward_small(name, w, cuda_device):
+    run_and_check(w, seed=1)
+    run_and_check(w, seed=2, with_dfinal=False, drop_D=w.D != "none")
+
+
+def test_backward_large_decay_and_long(cuda_device):
+    # dt scaled up (states forget within a few tokens) and a 1000-token sequence (31 checkpoints)
+    w = Workload("t", b=1, T=1000, H=2, P=64, N=128, G=1, Q=128, D="normal", init_std=0.1, seed=711)
+    run_and_check(w, seed=3, dt_scale=10.0)
+    run_and_check(w, seed=4)
+
+
+def test_backward_at_the_2p7b_head_dims(cuda_device):
+    """A medium case at the 2.7B layer's head dims (N 128, P 64, 8 heads per group)."""
+    w = Workload("t", b=1, T=512, H=8, P=64, N=128, G=1, Q=256, D="normal", seed=712)
+    run_and_check(w, seed=5)
+
+
+def test_backward_empty_and_rejections(cuda_device):
+    dev = cuda_device
+    x = torch.zeros((2, 0, 4, 64), device=dev, dtype=torch.bfloat16)
+    Bm = torch.zeros((2, 0, 1, 128), device=dev, dtype=torch.bfloat16)
+    dt = torch.zeros((2, 0, 4), device=dev)
+    A = -torch.ones(4, device=dev)
+    df = torch.randn((2, 4, 128, 64), device=dev)
+    g = ssd.ssd_bwd(x, dt, A, Bm, Bm.clone(), None, None, x.clone(), df)
+    torch.cuda.synchronize()
+    assert torch.equal(g["dinit"], df) and torch.count_nonzero(g["dA"]) == 0
+    # head dims above 128 and the tcgen05 path are not taken
+    for kw in (dict(P=256, N=64), dict(P=64, N=128, path="tcgen05")):
+        d = ssd.make_dims(1, 64, 2, kw["P"], kw["N"], 1, 128, path=kw.get("path", "auto"))
+        with pytest.raises(ssd.SSDError) as e:
+            ssd.ssd_bwd_workspace_size(d)
+        assert e.value.status == ssd.SSD_ERR_UNSUPPORTED
