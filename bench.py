@@ -91,6 +91,56 @@ def recorded_traffic(w, path):
     return int(fields["dram_bytes_per_launch"])
 
 
+def time_backward(ssd, torch, w, d, dev, stream, flush, peaks, args):
+    """ssd_bwd on the bench inputs: the whole call (checkpoints, reverse sweep, finishing kernels),
+    CUDA events on the launching stream, L2 flushed before each call; plus the fp64 backward
+    oracle on a bounded sample of the same workload on the host cores."""
+    from ssd_sequence_mixing_fwd_b300.inputs import algorithmic_bytes_bwd, make_inputs
+    g = torch.Generator(device="cpu").manual_seed(4242)
+    dy = torch.randn(d["x"].shape, generator=g).to(d["x"].dtype).to(dev)
+    b, T, H, P = d["x"].shape
+    N = d["B"].shape[3]
+    dfin = torch.randn((b, H, N, P), generator=g).to(dev)
+    dims = ssd.make_dims(b, T, H, P, N, d["B"].shape[2], w.Q, "scalar" if d["A"].dim() == 1 else "diagonal",
+                         "bf16" if d["x"].dtype == torch.bfloat16 else "f32")
+    ws = torch.empty(ssd.ssd_bwd_workspace_size(dims), device=dev, dtype=torch.uint8)
+    times = []
+    with torch.cuda.stream(stream):
+        for i in range(4):
+            flush.fill_(1.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            ssd.ssd_bwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["init_state"], dy, dfin, workspace=ws,
+                        stream=stream)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            if i >= 1:
+                times.append(e0.elapsed_time(e1))
+    ms = sum(times) / len(times)
+    by = algorithmic_bytes_bwd(w)
+    ent = {"path": "generic (CUDA cores)", "call_ms": ms, "tokens_per_s": w.tokens / (ms / 1e3),
+           "workspace_bytes": ws.numel(),
+           "roofline": {"bound": "hbm", "achieved": by / (ms / 1e3) / 1e9, "peak": peaks["hbm_gbs"],
+                        "unit": "GB/s", "frac": by / (ms / 1e3) / 1e9 / peaks["hbm_gbs"], "algorithmic_bytes": by},
+           "note": "3 calls after 1 warm-up; the call includes the checkpoint sweep, the reverse sweep, "
+                   "the finishing kernels and the workspace clears"}
+    if not args.no_cpu_baseline:
+        import time as _time
+        import oracle
+        ws_w = w.with_(b=1, T=min(w.T, 1024), H=min(w.H, 2), G=1)
+        inp = make_inputs(ws_w)
+        dyh = torch.randn((ws_w.b, ws_w.T, ws_w.H, ws_w.P), generator=g).double().numpy()
+        t0 = _time.perf_counter()
+        oracle.recurrence_bwd(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"], inp["init_state"],
+                              dyh, None)
+        sec = _time.perf_counter() - t0
+        ent["cpu_baseline"] = {"value": ws_w.tokens * ws_w.H / sec / w.H, "unit": "tokens/s (layer)",
+                               "cores": min(oracle.threads_used(), ws_w.H), "kind": "oracle",
+                               "sample": "b1 T%d, %d of %d heads, fp64 backward oracle; scaled to the layer's heads"
+                                         % (ws_w.T, ws_w.H, w.H)}
+    return ent
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -413,6 +463,8 @@ def run_ours(args, w):
                               "chunked_speedup": lin_ms / kern_ms,
                               "note": "ssd_scan on the same inputs, 3 launches after 1 warm-up; "
                                       "chunked_speedup = linear-form time / chunked kernel time"}
+        # the backward pass (ssd_bwd, CUDA cores) on the same inputs with random cotangents
+        out["backward"] = time_backward(ssd, torch, w, d, dev, stream, flush, peaks, args)
         # the other workloads the parity targets are quoted on, timed in the same run: kernel time,
         # roofline fraction, path, and the oracle on a bounded sample of each
         from ssd_sequence_mixing_fwd_b300.inputs import WORKLOAD_ORDER, WORKLOADS

@@ -15,15 +15,16 @@
 // dC, dA and dD are summed over the heads / batch rows that share them).  The
 // reverse sweep needs h_t and h_{t-1} at every token, so the states are
 // recomputed: a forward sweep stores the state at the start of every
-// 32-token block (checkpoints), and the reverse sweep recomputes each block's 32
+// 16-token block (checkpoints), and the reverse sweep recomputes each block's 16
 // states from its checkpoint into shared memory before walking it backwards.
 //
-// Work split: one CTA per (batch row, head, slice of R = 1024 / P state rows), 256
-// threads; thread t owns state row r = t / (P/4) of the slice and columns
-// 4 (t mod P/4) .. + 3, so a row's P columns are P/4 consecutive lanes of one warp
-// (P <= 128) and the sums over p are warp shuffles.  The sum over n for dx is
-// across rows: through shared memory within the CTA and fp32 atomics across
-// slices.  Per-token quantities that are summed over heads or over n later (dB,
+// Work split: one CTA per (batch row, head, slice of R = 1024 / P state rows);
+// thread t owns state row r = t / (P/W) of the slice and W = 4 consecutive columns,
+// so a row's P columns are P/W consecutive lanes of one warp (P <= 128) and the sums
+// over p are warp shuffles; 1024 / W = 256 threads.  The sum over n for dx is
+// across rows: a warp's rows are summed by shuffles, the warps' sums by
+// shared-memory atomics into the block's dx tile, and the tile goes to an fp32
+// accumulator once per block (atomics across slices).  Per-token quantities that are summed over heads or over n later (dB,
 // dC per head, dlog) go to workspace arrays; small kernels finish the sums and
 // convert to the io dtype.
 #include <cuda_bf16.h>
@@ -33,8 +34,7 @@
 namespace ssd {
 namespace {
 
-constexpr int kT = 256;      // threads per CTA
-constexpr int kK = 32;       // tokens per checkpoint block
+constexpr int kK = 16;       // tokens per checkpoint block
 constexpr int kElems = 1024; // state entries per CTA (R rows x P columns)
 
 template <typename IO> __device__ __forceinline__ float ldf(const IO *p, int64_t i);
@@ -67,115 +67,147 @@ __device__ __forceinline__ float decay_log(const BwdParams &p, int h, int n, flo
 
 // Stage kK tokens of one (batch row, head, slice): dt, x, B and C rows of the slice (and dy).
 template <typename IO, bool kDy>
-__device__ void stage(const BwdParams &p, int bi, int h, int sl, int t0, float *sdt, float *sx, float *sB,
+__device__ void stage(const BwdParams &p, int bi, int h, int sl, int t0, float *sa, float *sx, float *sB,
                       float *sC, float *sdy) {
     const int g = h / (p.H / p.G);
     const int L = min(kK, p.T - t0);
-    for (int i = threadIdx.x; i < kK; i += kT)
-        sdt[i] = i < L ? p.dt[((int64_t)bi * p.T + t0 + i) * p.H + h] : 0.f;
-    for (int i = threadIdx.x; i < kK * p.P; i += kT) {
+
+    for (int i = threadIdx.x; i < kK * p.P; i += blockDim.x) {
         const int k = i / p.P, c = i % p.P;
         const int64_t off = ((int64_t)bi * p.T + t0 + k) * p.H * p.P + (int64_t)h * p.P + c;
         sx[i] = k < L ? ldf(static_cast<const IO *>(p.x), off) : 0.f;
         if (kDy) sdy[i] = k < L ? ldf(static_cast<const IO *>(p.dy), off) : 0.f;
     }
-    for (int i = threadIdx.x; i < kK * p.R; i += kT) {
+    for (int i = threadIdx.x; i < kK * p.R; i += blockDim.x) {
         const int k = i / p.R, r = i % p.R, n = sl * p.R + r;
         const int64_t off = ((int64_t)bi * p.T + t0 + k) * p.G * p.N + (int64_t)g * p.N + n;
         const bool ok = k < L && n < p.N;
         sB[i] = ok ? ldf(static_cast<const IO *>(p.B), off) : 0.f;
         if (kDy) sC[i] = ok ? ldf(static_cast<const IO *>(p.C), off) : 0.f;
+        // the token's decay of this state row
+        sa[i] = ok ? expf(decay_log(p, h, n, p.dt[((int64_t)bi * p.T + t0 + k) * p.H + h])) : 0.f;
     }
 }
 
+template <int W> __device__ __forceinline__ void ld_w(const float *src, float (&v)[W]) {
+#pragma unroll
+    for (int j = 0; j < W; j += 4) {
+        const float4 f = *reinterpret_cast<const float4 *>(src + j);
+        v[j] = f.x; v[j + 1] = f.y; v[j + 2] = f.z; v[j + 3] = f.w;
+    }
+}
+template <int W> __device__ __forceinline__ void st_w(float *dst, const float (&v)[W]) {
+#pragma unroll
+    for (int j = 0; j < W; j += 4) *reinterpret_cast<float4 *>(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+}
+
 // Forward sweep: the state at the start of every kK-token block.
-template <typename IO>
-__global__ void __launch_bounds__(kT) bwd_ckpt_kernel(BwdParams p) {
-    __shared__ float sdt[kK];
+template <typename IO, int W>
+__global__ void __launch_bounds__(kElems / W) bwd_ckpt_kernel(BwdParams p) {
     extern __shared__ float sm[];
-    float *sx = sm, *sB = sx + kK * p.P;
+    float *sx = sm, *sB = sx + kK * p.P, *sa = sB + kK * p.R;
     const int nsl = p.nsl;
     const int sl = blockIdx.x % nsl, s = blockIdx.x / nsl;
     const int bi = s / p.H, h = s % p.H;
-    const int tpr = p.P / 4, r = threadIdx.x / tpr, p0 = 4 * (threadIdx.x % tpr);
+    const int tpr = p.P / W, r = threadIdx.x / tpr, p0 = W * (threadIdx.x % tpr);
     const int n = sl * p.R + r;
     const bool live = n < p.N;
-    float hs[4];
+    float hs[W];
+    if (p.init && live) ld_w<W>(p.init + ((int64_t)s * p.N + n) * p.P + p0, hs);
+    else {
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-        hs[j] = (p.init && live) ? p.init[((int64_t)s * p.N + n) * p.P + p0 + j] : 0.f;
+        for (int j = 0; j < W; ++j) hs[j] = 0.f;
+    }
     float *ck = p.ck + ((int64_t)s * nsl + sl) * p.nK * kElems;
     for (int kb = 0; kb < p.nK; ++kb) {
-        *reinterpret_cast<float4 *>(ck + (int64_t)kb * kElems + r * p.P + p0) = make_float4(hs[0], hs[1], hs[2], hs[3]);
+        st_w<W>(ck + (int64_t)kb * kElems + r * p.P + p0, hs);
         __syncthreads();
-        stage<IO, false>(p, bi, h, sl, kb * kK, sdt, sx, sB, nullptr, nullptr);
+        stage<IO, false>(p, bi, h, sl, kb * kK, sa, sx, sB, nullptr, nullptr);
         __syncthreads();
         const int L = min(kK, p.T - kb * kK);
+#pragma unroll 4
         for (int k = 0; k < L; ++k) {
-            const float a = live ? expf(decay_log(p, h, n, sdt[k])) : 0.f;
+            const float a = sa[k * p.R + r];
             const float bn = sB[k * p.R + r];
+            float xv[W];
+            ld_w<W>(sx + k * p.P + p0, xv);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) hs[j] = fmaf(a, hs[j], bn * sx[k * p.P + p0 + j]);
+            for (int j = 0; j < W; ++j) hs[j] = fmaf(a, hs[j], bn * xv[j]);
         }
     }
 }
 
 // Reverse sweep.
-template <typename IO>
-__global__ void __launch_bounds__(kT) bwd_reverse_kernel(BwdParams p) {
-    __shared__ float sdt[kK];
+template <typename IO, int W>
+__global__ void __launch_bounds__(kElems / W) bwd_reverse_kernel(BwdParams p) {
     extern __shared__ float sm[];
     float *hb = sm;                               // [kK + 1][kElems]: h_{t0-1} .. h_{t0+kK-1}
     float *sx = hb + (kK + 1) * kElems;           // [kK][P]
     float *sdy = sx + kK * p.P;                   // [kK][P]
     float *sB = sdy + kK * p.P;                   // [kK][R]
     float *sC = sB + kK * p.R;                    // [kK][R]
-    float *red = sC + kK * p.R;                   // [R][P] partial dx
+    float *sa = sC + kK * p.R;                    // [kK][R] decays
+    float *red = sa + kK * p.R;                   // [kK][P] the block's dx over this slice's rows
     const int nsl = p.nsl;
     const int sl = blockIdx.x % nsl, s = blockIdx.x / nsl;
     const int bi = s / p.H, h = s % p.H;
-    const int tpr = p.P / 4, r = threadIdx.x / tpr, p0 = 4 * (threadIdx.x % tpr);
+    const int tpr = p.P / W, r = threadIdx.x / tpr, p0 = W * (threadIdx.x % tpr);
     const int n = sl * p.R + r;
     const bool live = n < p.N;
-    float gr[4];
+    float gr[W];
+    if (p.dfinal && live) ld_w<W>(p.dfinal + ((int64_t)s * p.N + n) * p.P + p0, gr);
+    else {
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-        gr[j] = (p.dfinal && live) ? p.dfinal[((int64_t)s * p.N + n) * p.P + p0 + j] : 0.f;
+        for (int j = 0; j < W; ++j) gr[j] = 0.f;
+    }
     const float *ck = p.ck + ((int64_t)s * nsl + sl) * p.nK * kElems;
     for (int kb = p.nK - 1; kb >= 0; --kb) {
         const int t0 = kb * kK, L = min(kK, p.T - t0);
         __syncthreads();
-        stage<IO, true>(p, bi, h, sl, t0, sdt, sx, sB, sC, sdy);
-        float hs[4];
-        {
-            const float4 v = *reinterpret_cast<const float4 *>(ck + (int64_t)kb * kElems + r * p.P + p0);
-            hs[0] = v.x; hs[1] = v.y; hs[2] = v.z; hs[3] = v.w;
-        }
+        stage<IO, true>(p, bi, h, sl, t0, sa, sx, sB, sC, sdy);
+        for (int i = threadIdx.x; i < kK * p.P; i += blockDim.x) red[i] = 0.f;
+        float hs[W];
+        ld_w<W>(ck + (int64_t)kb * kElems + r * p.P + p0, hs);
         __syncthreads();
-        *reinterpret_cast<float4 *>(hb + r * p.P + p0) = make_float4(hs[0], hs[1], hs[2], hs[3]);
+        st_w<W>(hb + r * p.P + p0, hs);
+#pragma unroll 4
         for (int k = 0; k < L; ++k) {
-            const float a = live ? expf(decay_log(p, h, n, sdt[k])) : 0.f;
+            const float a = sa[k * p.R + r];
             const float bn = sB[k * p.R + r];
+            float xv[W];
+            ld_w<W>(sx + k * p.P + p0, xv);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) hs[j] = fmaf(a, hs[j], bn * sx[k * p.P + p0 + j]);
-            *reinterpret_cast<float4 *>(hb + (k + 1) * kElems + r * p.P + p0) = make_float4(hs[0], hs[1], hs[2], hs[3]);
+            for (int j = 0; j < W; ++j) hs[j] = fmaf(a, hs[j], bn * xv[j]);
+            st_w<W>(hb + (k + 1) * kElems + r * p.P + p0, hs);
         }
+#pragma unroll 2
         for (int k = L - 1; k >= 0; --k) {
             const int t = t0 + k;
-            const float a = live ? expf(decay_log(p, h, n, sdt[k])) : 0.f;
+            const float a = sa[k * p.R + r];
             const float cn = sC[k * p.R + r], bn = sB[k * p.R + r];
-            const float4 hc = *reinterpret_cast<const float4 *>(hb + (k + 1) * kElems + r * p.P + p0);
-            const float4 hp = *reinterpret_cast<const float4 *>(hb + k * kElems + r * p.P + p0);
-            const float hcv[4] = {hc.x, hc.y, hc.z, hc.w}, hpv[4] = {hp.x, hp.y, hp.z, hp.w};
-            float c = 0.f, b = 0.f, l = 0.f;
+            float hcv[W], hpv[W], dyv[W], xv[W];
+            ld_w<W>(hb + (k + 1) * kElems + r * p.P + p0, hcv);
+            ld_w<W>(hb + k * kElems + r * p.P + p0, hpv);
+            ld_w<W>(sdy + k * p.P + p0, dyv);
+            ld_w<W>(sx + k * p.P + p0, xv);
+            float c = 0.f, b = 0.f, l = 0.f, xs[W];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float dyv = sdy[k * p.P + p0 + j];
-                gr[j] = fmaf(cn, dyv, gr[j]);
-                c = fmaf(hcv[j], dyv, c);
-                b = fmaf(gr[j], sx[k * p.P + p0 + j], b);
+            for (int j = 0; j < W; ++j) {
+                gr[j] = fmaf(cn, dyv[j], gr[j]);
+                c = fmaf(hcv[j], dyv[j], c);
+                b = fmaf(gr[j], xv[j], b);
                 l = fmaf(gr[j], hpv[j], l);
-                red[r * p.P + p0 + j] = bn * gr[j];
+                xs[j] = bn * gr[j];
+            }
+            // dx over this slice's rows: the warp's rows (lanes tpr apart hold the same columns)
+            // by shuffles, the warps by shared-memory atomics
+            for (int o = tpr; o < 32; o <<= 1) {
+#pragma unroll
+                for (int j = 0; j < W; ++j) xs[j] += __shfl_xor_sync(0xffffffffu, xs[j], o);
+            }
+            if ((threadIdx.x & 31) < tpr) {
+#pragma unroll
+                for (int j = 0; j < W; ++j) atomicAdd(red + k * p.P + p0 + j, xs[j]);
             }
             // (offsets below tpr stay inside the row's aligned group of tpr lanes)
             for (int o = tpr >> 1; o >= 1; o >>= 1) {
@@ -189,19 +221,16 @@ __global__ void __launch_bounds__(kT) bwd_reverse_kernel(BwdParams p) {
                 p.dBh[o] = b;
                 p.dl[o] = a * l;
             }
-            __syncthreads();
-            for (int c2 = threadIdx.x; c2 < p.P; c2 += kT) {
-                float acc = 0.f;
-                for (int rr = 0; rr < p.R; ++rr) acc += red[rr * p.P + c2];
-                atomicAdd(p.dxa + (((int64_t)bi * p.T + t) * p.H + h) * p.P + c2, acc);
-            }
-            __syncthreads();
 #pragma unroll
-            for (int j = 0; j < 4; ++j) gr[j] *= a;
+            for (int j = 0; j < W; ++j) gr[j] *= a;
+        }
+        __syncthreads();
+        for (int i = threadIdx.x; i < L * p.P; i += blockDim.x) {
+            const int k = i / p.P, c2 = i % p.P;
+            atomicAdd(p.dxa + (((int64_t)bi * p.T + t0 + k) * p.H + h) * p.P + c2, red[i]);
         }
     }
-    if (p.dinit && live)
-        *reinterpret_cast<float4 *>(p.dinit + ((int64_t)s * p.N + n) * p.P + p0) = make_float4(gr[0], gr[1], gr[2], gr[3]);
+    if (p.dinit && live) st_w<W>(p.dinit + ((int64_t)s * p.N + n) * p.P + p0, gr);
 }
 
 // dx = accumulated sum (+ D dy) in the io dtype; ddt = sum_n A_n dlog.
@@ -244,14 +273,17 @@ __global__ void bwd_finish_bc(BwdParams p) {
 }
 
 // dA (sum over batch rows and tokens of dt dlog; over n too for scalar A) and dD (sum of dy x):
-// one CTA per head and (diagonal A) per state row, a block-wide reduction.
+// CTA (head, state row or 0, chunk of kChunk tokens), a block-wide sum added atomically into the
+// zeroed outputs.
+constexpr int kChunk = 1024;
 template <typename IO>
-__global__ void bwd_finish_params(BwdParams p) {
-    __shared__ float part[2][kT / 32];
+__global__ void __launch_bounds__(256) bwd_finish_params(BwdParams p) {
+    __shared__ float part[2][8];
     const int h = blockIdx.x, k = blockIdx.y;     // k: state row (diagonal A), else 0
     float sa = 0.f, sd = 0.f;
     const int64_t nbt = (int64_t)p.b * p.T;
-    for (int64_t bt = threadIdx.x; bt < nbt; bt += blockDim.x) {
+    const int64_t b0 = (int64_t)blockIdx.z * kChunk, b1 = min(nbt, b0 + kChunk);
+    for (int64_t bt = b0 + threadIdx.x; bt < b1; bt += blockDim.x) {
         const int64_t tok = bt * p.H + h;
         const float dtv = p.dt[tok];
         if (p.diag) {
@@ -276,12 +308,12 @@ __global__ void bwd_finish_params(BwdParams p) {
     __syncthreads();
     if (threadIdx.x == 0) {
         float a = 0.f, d = 0.f;
-        for (int w = 0; w < kT / 32; ++w) {
+        for (int w = 0; w < 8; ++w) {
             a += part[0][w];
             d += part[1][w];
         }
-        p.dA[p.diag ? (int64_t)h * p.N + k : h] = a;
-        if (k == 0 && p.dD) p.dD[h] = d;
+        atomicAdd(p.dA + (p.diag ? (int64_t)h * p.N + k : h), a);
+        if (k == 0 && p.dD) atomicAdd(p.dD + h, d);
     }
 }
 
@@ -306,23 +338,33 @@ BwdLayout bwd_layout(const Problem &p) {
 }
 
 size_t reverse_smem(const Problem &p, const BwdLayout &l) {
-    return sizeof(float) * ((size_t)(kK + 1) * kElems + 2 * kK * p.P + 2 * kK * l.R + (size_t)l.R * p.P);
+    return sizeof(float) * ((size_t)(kK + 1) * kElems + 3 * kK * p.P + 3 * kK * l.R);
+}
+
+template <typename IO, int W>
+cudaError_t launch_sweeps(const Problem &p, const BwdParams &bp, const BwdLayout &l, cudaStream_t s) {
+    const size_t sm_ck = sizeof(float) * (size_t)(kK * p.P + 2 * kK * l.R);
+    const size_t sm_rev = reverse_smem(p, l);
+    cudaError_t e = cudaFuncSetAttribute(bwd_reverse_kernel<IO, W>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_rev);
+    if (e != cudaSuccess) return e;
+    const unsigned grid = (unsigned)(p.b * p.H * l.nsl);
+    record_dominant_start(s);
+    bwd_ckpt_kernel<IO, W><<<grid, kElems / W, sm_ck, s>>>(bp);
+    bwd_reverse_kernel<IO, W><<<grid, kElems / W, sm_rev, s>>>(bp);
+    record_dominant_stop(s);
+    return cudaGetLastError();
 }
 
 template <typename IO>
 cudaError_t launch_all(const Problem &p, const BwdParams &bp, const BwdLayout &l, cudaStream_t s) {
-    const size_t sm_ck = sizeof(float) * (size_t)(kK * p.P + kK * l.R);
-    const size_t sm_rev = reverse_smem(p, l);
-    cudaError_t e = cudaFuncSetAttribute(bwd_reverse_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_rev);
+    // four columns per thread (256 threads): eight (128 threads) measured slower -- fewer warps to
+    // hide the per-token latency
+    cudaError_t e = launch_sweeps<IO, 4>(p, bp, l, s);
     if (e != cudaSuccess) return e;
-    const unsigned grid = (unsigned)(p.b * p.H * l.nsl);
-    record_dominant_start(s);
-    bwd_ckpt_kernel<IO><<<grid, kT, sm_ck, s>>>(bp);
-    bwd_reverse_kernel<IO><<<grid, kT, sm_rev, s>>>(bp);
-    record_dominant_stop(s);
     bwd_finish_tokens<IO><<<1184, 256, 0, s>>>(bp);
     bwd_finish_bc<IO><<<1184, 256, 0, s>>>(bp);
-    bwd_finish_params<IO><<<dim3((unsigned)p.H, bp.diag ? (unsigned)p.N : 1u), kT, 0, s>>>(bp);
+    const unsigned chunks = (unsigned)((p.b * p.T + kChunk - 1) / kChunk);
+    bwd_finish_params<IO><<<dim3((unsigned)p.H, bp.diag ? (unsigned)p.N : 1u, chunks), 256, 0, s>>>(bp);
     note_launches(5);
     return cudaGetLastError();
 }
@@ -331,6 +373,7 @@ cudaError_t launch_all(const Problem &p, const BwdParams &bp, const BwdLayout &l
 
 bool bwd_supports(const Problem &p) {
     if (p.P < 4 || p.P > 128 || (p.P & (p.P - 1))) return false;   // a state row's columns within one warp
+    if ((p.b * p.T + kChunk - 1) / kChunk > 65535) return false;     // grid z of the parameter sums
     if (p.b * p.H * ((p.N + kElems / p.P - 1) / (kElems / p.P)) > (int64_t)INT32_MAX) return false;
     if (p.T > (int64_t)INT32_MAX / 2) return false;
     return true;
@@ -356,6 +399,9 @@ cudaError_t bwd_launch(const Problem &p, const BwdGrads &gr, void *ws, cudaStrea
     bp.diag = p.a_mode == SSD_A_DIAGONAL;
     cudaError_t e = cudaMemsetAsync(base, 0, kStatusBytes, s);
     if (e == cudaSuccess) e = cudaMemsetAsync(bp.dxa, 0, sizeof(float) * (size_t)(p.b * p.T * p.H * p.P), s);
+    if (e == cudaSuccess)
+        e = cudaMemsetAsync(gr.dA, 0, sizeof(float) * (size_t)(p.a_mode == SSD_A_SCALAR ? p.H : p.H * p.N), s);
+    if (e == cudaSuccess && gr.dD) e = cudaMemsetAsync(gr.dD, 0, sizeof(float) * (size_t)p.H, s);
     if (e != cudaSuccess) return e;
     return p.io_dtype == SSD_DTYPE_BF16 ? launch_all<__nv_bfloat16>(p, bp, l, s) : launch_all<float>(p, bp, l, s);
 }

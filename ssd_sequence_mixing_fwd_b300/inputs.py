@@ -112,6 +112,19 @@ def algorithmic_bytes(w: Workload, final_state=True) -> int:
     return by
 
 
+def algorithmic_bytes_bwd(w: Workload) -> int:
+    """HBM floor of one backward call: x, dy, B, C, dt (and init_state, dfinal) read once; dx, dB,
+    dC, ddt (and dinit) written once; dA and dD are negligible."""
+    e = 2 if w.dtype == "bf16" else 4
+    tok = w.b * w.T
+    by = tok * w.H * w.P * e * 3                 # x, dy in; dx out
+    by += tok * w.G * w.N * e * 4                # B, C in; dB, dC out
+    by += tok * w.H * 4 * 2                      # dt in, ddt out
+    st = w.b * w.H * w.N * w.P * 4
+    by += st * (2 if w.init_std > 0 else 1) + st  # init (if any), dfinal in; dinit out
+    return by
+
+
 def algorithmic_flops(w: Workload) -> float:
     """Causal tensor-core work of the chunked algorithm (elementwise work excluded).
 
