@@ -211,7 +211,7 @@ SSD_API int ssd_decode_step(const ssd_dims *dims,
  * weighs; the pages give no backward, so this is the chain rule of the
  * recurrence of "The recurrence as one matrix").  CUDA cores, fp32
  * arithmetic: a forward sweep stores the state at the start of every
- * 16-token block, and a reverse sweep recomputes each block's states from it
+ * 8-token block, and a reverse sweep recomputes each block's states from it
  * while it runs the adjoint recurrence g = C_t dy_t^T + a_{t+1} (.) g.
  *
  * Inputs (device memory, layouts of ssd_fwd): x, dt, A, B, C, D (or NULL),
@@ -225,7 +225,7 @@ SSD_API int ssd_decode_step(const ssd_dims *dims,
  * dims->path must be SSD_PATH_AUTO or SSD_PATH_GENERIC (SSD_ERR_UNSUPPORTED
  * otherwise); the backward takes 4 <= P <= 128.  Every pointer 16-byte
  * aligned; workspace >= ssd_bwd_workspace_size bytes, 256-byte aligned
- * (checkpoints b*H*ceil(N/(1024/P))*ceil(T/16)*4 KB plus fp32 per-token
+ * (checkpoints b*H*ceil(N/(1024/P))*ceil(T/8)*4 KB plus fp32 per-token
  * arrays of 3*b*T*H*N + b*T*H*P floats).  Asynchronous on `stream`; on any
  * argument error nothing is enqueued.  b == 0 or T == 0: dA and dD are zero
  * and dinit is dfinal (or zero). */

@@ -15,8 +15,9 @@
 // dC, dA and dD are summed over the heads / batch rows that share them).  The
 // reverse sweep needs h_t and h_{t-1} at every token, so the states are
 // recomputed: a forward sweep stores the state at the start of every
-// 16-token block (checkpoints), and the reverse sweep recomputes each block's 16
-// states from its checkpoint into shared memory before walking it backwards.
+// 8-token block (checkpoints), and the reverse sweep recomputes each block's 8
+// states from its checkpoint into shared memory before walking it backwards
+// (short blocks: four CTAs per SM).
 //
 // Work split: one CTA per (batch row, head, slice of R = 1024 / P state rows);
 // thread t owns state row r = t / (P/W) of the slice and W = 4 consecutive columns,
@@ -34,7 +35,7 @@
 namespace ssd {
 namespace {
 
-constexpr int kK = 16;       // tokens per checkpoint block
+constexpr int kK = 8;        // tokens per checkpoint block
 constexpr int kElems = 1024; // state entries per CTA (R rows x P columns)
 
 template <typename IO> __device__ __forceinline__ float ldf(const IO *p, int64_t i);
