@@ -91,6 +91,33 @@ def recorded_traffic(w, path):
     return int(fields["dram_bytes_per_launch"])
 
 
+def time_decode(ssd, torch, w, d, dev, stream, peaks):
+    """ssd_decode_step on one token per sequence of the bench workload's batch and heads, the
+    state (b,H,N,P) fp32 read and written in place; 20 steps after 5 warm-ups, CUDA events."""
+    b, T, H, P = d["x"].shape
+    N = d["B"].shape[3]
+    x1, dt1, B1, C1 = (d[k][:, :1].contiguous() for k in ("x", "dt", "B", "C"))
+    state = torch.zeros((b, H, N, P), device=dev, dtype=torch.float32)
+    y1 = torch.empty_like(x1)
+    for _ in range(5):
+        ssd.ssd_decode_step(x1, dt1, d["A"], B1, C1, d["D"], state, y=y1, stream=stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    steps = 20
+    e0.record(stream)
+    for _ in range(steps):
+        ssd.ssd_decode_step(x1, dt1, d["A"], B1, C1, d["D"], state, y=y1, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / steps
+    e = x1.element_size()
+    by = 2 * state.numel() * 4 + 2 * x1.numel() * e + 2 * B1.numel() * e + dt1.numel() * 4
+    return {"step_ms": ms, "tokens_per_s": b / (ms / 1e3), "batch": b,
+            "roofline": {"bound": "hbm", "achieved": by / (ms / 1e3) / 1e9, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": by / (ms / 1e3) / 1e9 / peaks["hbm_gbs"], "bytes": by},
+            "note": "one generated token for each of the batch's sequences per step (state read and written "
+                    "in place; the state stays in L2 between steps at this size), 20 steps after 5 warm-ups"}
+
+
 def time_backward(ssd, torch, w, d, dev, stream, flush, peaks, args):
     """ssd_bwd on the bench inputs: the whole call (checkpoints, reverse sweep, finishing kernels),
     CUDA events on the launching stream, L2 flushed before each call; plus the fp64 backward
@@ -461,8 +488,13 @@ def run_ours(args, w):
         lin_ms = sum(lin) / len(lin)
         out["linear_form"] = {"kernel_ms": lin_ms, "tokens_per_s": w.tokens / (lin_ms / 1e3),
                               "chunked_speedup": lin_ms / kern_ms,
+                              "roofline": {"bound": "hbm", "achieved": by / (lin_ms / 1e3) / 1e9,
+                                           "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                           "frac": by / (lin_ms / 1e3) / 1e9 / peaks["hbm_gbs"]},
                               "note": "ssd_scan on the same inputs, 3 launches after 1 warm-up; "
-                                      "chunked_speedup = linear-form time / chunked kernel time"}
+                                      "chunked_speedup = linear-form time / chunked kernel time; the oracle "
+                                      "(cpu_baseline) is this same recurrence in fp64"}
+        out["decode_step"] = time_decode(ssd, torch, w, d, dev, stream, peaks)
         # the backward pass (ssd_bwd, CUDA cores) on the same inputs with random cotangents
         out["backward"] = time_backward(ssd, torch, w, d, dev, stream, flush, peaks, args)
         # the other workloads the parity targets are quoted on, timed in the same run: kernel time,
