@@ -156,6 +156,79 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(Problem p) {
     }
 }
 
+// One token (T = 1: the decode step, and ssd_scan at T = 1): the state read and written in
+// 16-byte pieces.  One CTA per (batch row, head), 256 threads; thread t updates the float4s
+// e = t + 256 k of the N x P/4 state (row e / (P/4), columns 4 (e mod P/4) ..), all in the same
+// columns, so its part of C^T h is four sums; the parts are summed over a warp's rows by
+// shuffles and over the warps through shared memory.
+constexpr int kDecThreads = 256;
+
+template <typename IO, bool kDiag>
+__global__ void __launch_bounds__(kDecThreads) decode_kernel(Problem p) {
+    __shared__ float sB[256], sC[256], sa[256];
+    __shared__ float sx[256], part[kDecThreads / 32][256];
+    const int P = (int)p.P, N = (int)p.N, H = (int)p.H;
+    const int P4 = P / 4;
+    const int bi = blockIdx.x / H, h = blockIdx.x % H;
+    const int g = h / (H / (int)p.G);
+    const int64_t sidx = (int64_t)bi * H + h;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const float dtv = p.dt[(int64_t)bi * H + h];
+    for (int i = tid; i < N; i += kDecThreads) {
+        const int64_t off = ((int64_t)bi * p.G + g) * N + i;
+        sB[i] = ld_io(static_cast<const IO *>(p.B), off);
+        sC[i] = ld_io(static_cast<const IO *>(p.C), off);
+        sa[i] = kDiag ? expf(dtv * p.A[(int64_t)h * N + i]) : 0.f;
+    }
+    for (int i = tid; i < P; i += kDecThreads) sx[i] = ld_io(static_cast<const IO *>(p.x), sidx * P + i);
+    const float a_s = kDiag ? 0.f : expf(dtv * p.A[h]);
+    __syncthreads();
+    const int p4 = tid % P4;
+    float x4[4], y4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) x4[j] = sx[4 * p4 + j];
+    const float4 *src = p.init ? reinterpret_cast<const float4 *>(p.init + sidx * N * P) : nullptr;
+    float4 *dst = reinterpret_cast<float4 *>(p.final_state + sidx * N * P);
+    for (int e = tid; e < N * P4; e += kDecThreads) {
+        const int n = e / P4;
+        const float a = kDiag ? sa[n] : a_s, bn = sB[n], cn = sC[n];
+        const float4 hv = src ? src[e] : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 nv = make_float4(fmaf(a, hv.x, bn * x4[0]), fmaf(a, hv.y, bn * x4[1]),
+                                      fmaf(a, hv.z, bn * x4[2]), fmaf(a, hv.w, bn * x4[3]));
+        dst[e] = nv;
+        y4[0] = fmaf(cn, nv.x, y4[0]);
+        y4[1] = fmaf(cn, nv.y, y4[1]);
+        y4[2] = fmaf(cn, nv.z, y4[2]);
+        y4[3] = fmaf(cn, nv.w, y4[3]);
+    }
+    // lanes P4 apart hold the same columns
+    for (int o = P4; o < 32; o <<= 1) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) y4[j] += __shfl_xor_sync(0xffffffffu, y4[j], o);
+    }
+    if (lane < P4) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) part[warp][4 * lane + j] = y4[j];
+    }
+    __syncthreads();
+    const float Dh = p.D ? p.D[h] : 0.f;
+    for (int c = tid; c < P; c += kDecThreads) {
+        float acc = Dh * sx[c];
+#pragma unroll
+        for (int w = 0; w < kDecThreads / 32; ++w) acc += part[w][c];
+        st_io(static_cast<IO *>(p.y), sidx * P + c, acc);
+    }
+}
+
+// The one-token kernel applies: 4 <= P <= 128 (a row's columns within one warp), N <= 256, and
+// 16-byte aligned states.
+bool decode_applies(const Problem &p) {
+    if (p.T != 1 || !p.final_state || p.P < 4 || p.P > 128 || p.N > 256) return false;
+    if ((reinterpret_cast<uintptr_t>(p.final_state) & 15u) != 0) return false;
+    if (p.init && (reinterpret_cast<uintptr_t>(p.init) & 15u) != 0) return false;
+    return true;
+}
+
 template <typename IO, bool kDiag>
 cudaError_t launch_ns(const Problem &p, cudaStream_t s) {
     const int64_t ns = scan_rows(p);
@@ -192,6 +265,20 @@ bool scan_supports(const Problem &p) {
 
 cudaError_t scan_launch(const Problem &p, cudaStream_t s) {
     const bool diag = p.a_mode == SSD_A_DIAGONAL;
+    if (decode_applies(p)) {
+        const unsigned grid = (unsigned)(p.b * p.H);
+        record_dominant_start(s);
+        if (p.io_dtype == SSD_DTYPE_BF16) {
+            if (diag) decode_kernel<__nv_bfloat16, true><<<grid, kDecThreads, 0, s>>>(p);
+            else decode_kernel<__nv_bfloat16, false><<<grid, kDecThreads, 0, s>>>(p);
+        } else {
+            if (diag) decode_kernel<float, true><<<grid, kDecThreads, 0, s>>>(p);
+            else decode_kernel<float, false><<<grid, kDecThreads, 0, s>>>(p);
+        }
+        record_dominant_stop(s);
+        note_launches(1);
+        return cudaGetLastError();
+    }
     if (p.io_dtype == SSD_DTYPE_BF16)
         return diag ? launch_ns<__nv_bfloat16, true>(p, s) : launch_ns<__nv_bfloat16, false>(p, s);
     return diag ? launch_ns<float, true>(p, s) : launch_ns<float, false>(p, s);

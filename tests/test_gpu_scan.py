@@ -117,3 +117,25 @@ def test_decode_step_rejects_more_than_one_token(cuda_device):
     st = lib.ssd_decode_step(ctypes.byref(dims), *fake, None, ctypes.c_void_p(state.data_ptr()),
                              ctypes.c_void_p(state.data_ptr() + 4096), None)
     assert st == ssd.SSD_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("aligned", [True, False], ids=["one_token_kernel", "unaligned_state_fallback"])
+@pytest.mark.parametrize("a_mode", ["scalar", "diagonal"])
+def test_decode_steps_both_state_alignments(aligned, a_mode, cuda_device):
+    """Decode steps on a 16-byte aligned state (the one-token kernel) and on a state that starts 4
+    bytes into its buffer (the general kernel), against the oracle over the whole sequence."""
+    w = Workload("t", b=3, T=20, H=4, P=32, N=64 if a_mode == "diagonal" else 48, G=2, Q=64, a_mode=a_mode,
+                 D="normal", init_std=0.2, seed=541)
+    inp = make_inputs(w)
+    d = _dev(inp, cuda_device)
+    n = w.b * w.H * w.N * w.P
+    buf = torch.empty(n + 4, device=cuda_device, dtype=torch.float32)
+    state = buf[:n] if aligned else buf[1:n + 1]
+    state.view(w.b, w.H, w.N, w.P).copy_(d["init_state"])
+    st4 = state.view(w.b, w.H, w.N, w.P)
+    ys = []
+    for t in range(w.T):
+        ys.append(ssd.ssd_decode_step(d["x"][:, t:t + 1].contiguous(), d["dt"][:, t:t + 1].contiguous(), d["A"],
+                                      d["B"][:, t:t + 1].contiguous(), d["C"][:, t:t + 1].contiguous(), d["D"], st4))
+    torch.cuda.synchronize()
+    check(w, inp, torch.cat(ys, dim=1), st4)
