@@ -30,6 +30,8 @@
 // convert to the io dtype.
 #include <cuda_bf16.h>
 
+#include <cstring>
+
 #include "ssd_internal.cuh"
 
 namespace ssd {
@@ -318,6 +320,391 @@ __global__ void __launch_bounds__(256) bwd_finish_params(BwdParams p) {
     }
 }
 
+// ---- chunked backward (scalar A) ---------------------------------------------------
+// The same gradients, chunk by chunk as dense products: the chunked algorithm of
+// Structured State Space Duality, "The chunked algorithm takes both", run backwards (the
+// quadratic form inside each chunk, the state between chunks), which replaces the
+// per-token sums of the reverse sweep (one over p per state row, one over n per column:
+// shuffles and shared-memory atomics at every token) with products over whole chunks.
+// With Q-token chunks, cum the in-chunk prefix sum of dt A, L_ij = e^{cum_i - cum_j}
+// (j <= i, else 0), w_j = e^{cum_Q - cum_j}, e_i = e^{cum_i} (all <= 1), h the state
+// entering the chunk and g = dL/dh at its end:
+//   S = L o (C B^T),  G = L o (dY X^T)
+//   dX = S^T dY + w o (B g) + D dY
+//   dC = G B + e o (dY h^T),  dB = G^T C + w o (X g^T)
+//   the adjoint entering the chunk: e^{cum_Q} g + C^T (e o dY)
+//   with K = G o (C B^T), v_j = x_j.(B g)_j and u_i = C_i.(h dY_i), the gradient with respect
+//   to the in-chunk prefix sums, summed over i >= k, is
+//     rc_k = e^{cum_Q} <g, h> + sum_{j<k} w_j v_j + sum_{i>=k, j<k} K_ij + sum_{i>=k} e_i u_i
+//   (the pairs of K with both indices >= k, and the w v terms of tokens >= k, cancel exactly
+//   and are left out rather than summed and subtracted: at fp32 that difference lost a
+//   decade of dA's digits), and ddt_k = A rc_k, dA += sum_k dt_k rc_k.
+// Kernels: the generic forward's first two give the state entering every chunk;
+// bwd_chunk_r forms C^T (e o dY) per chunk; bwd_state_reverse runs the adjoint backwards
+// over the chunks (each chunk's end adjoint left in place, and dinit); bwd_chunk_grad does
+// the rest, one CTA per chunk and head, every product in exact fp32 on the CUDA cores.
+constexpr int kQc = 64;           // tokens per chunk
+constexpr int kCT = 256;          // threads of the chunk kernels
+
+struct BwdCParams {
+    const void *x, *B, *C, *dy;
+    const float *dt, *A, *D, *dfinal;
+    void *dx;
+    float *ddt, *dA, *dD, *dinit;
+    const float *states;   // (b, H, nc, N, P): the state entering each chunk
+    const float *csum;     // (b, H, nc): sum of dt A over each chunk
+    float *gst;            // (b, H, nc, N, P): C^T (e o dY), then the adjoint at each chunk's end
+    float *dBh, *dCh;      // (b, T, H, N) per head
+    int b, T, H, G, N, P, nc;
+};
+
+// cum[0..Q): inclusive prefix sum of dt A over the chunk (dt of token k at dt[k * stride];
+// zero past L, so the sum holds its last value there).  All threads of the block.
+__device__ __forceinline__ void chunk_cum(const float *dt, int64_t stride, float Ah, int L, float *cum) {
+    if (threadIdx.x < kQc) {
+        const int i = threadIdx.x;
+        float v = i < L ? dt[i * stride] * Ah : 0.f;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float u = __shfl_up_sync(0xffffffffu, v, o);
+            if ((i & 31) >= o) v += u;
+        }
+        cum[i] = v;
+    }
+    __syncthreads();
+    if (threadIdx.x >= 32 && threadIdx.x < kQc) cum[threadIdx.x] += cum[31];
+    __syncthreads();
+}
+
+// dst[k * ds + c] = src[base + k * rs + c] (fp32) for k < valid, 0 for valid <= k < rows.
+template <typename IO>
+__device__ __forceinline__ void load_rows(float *dst, int ds, const IO *src, int64_t base, int64_t rs, int rows,
+                                          int valid, int cols) {
+    for (int e = threadIdx.x; e < rows * cols; e += blockDim.x) {
+        const int k = e / cols, c = e % cols;
+        dst[k * ds + c] = k < valid ? ldf(src, base + k * rs + c) : 0.f;
+    }
+}
+
+// r = C^T (e o dY) of one chunk into gst.  Thread: column q of the state and R = N P / 256
+// consecutive state rows; the e o C rows are read as float4 broadcasts.
+template <typename IO, int N, int P>
+__global__ void __launch_bounds__(kCT) bwd_chunk_r(BwdCParams p) {
+    constexpr int Q = kQc, R = N * P / kCT;
+    extern __shared__ float sm[];
+    float *sCe = sm;                  // [Q][N]
+    float *sdY = sCe + Q * N;         // [Q][P]
+    float *cum = sdY + Q * P;         // [Q]
+    float *ev = cum + Q;              // [Q]
+    const int c = blockIdx.x, h = blockIdx.y, bi = blockIdx.z, tid = threadIdx.x;
+    const int64_t t0 = (int64_t)c * Q;
+    const int L = (int)min((int64_t)Q, (int64_t)p.T - t0);
+    const int g = h / (p.H / p.G);
+    const int64_t tok0 = (int64_t)bi * p.T + t0;
+    load_rows(sdY, P, static_cast<const IO *>(p.dy), tok0 * p.H * P + (int64_t)h * P, (int64_t)p.H * P, Q, L, P);
+    chunk_cum(p.dt + tok0 * p.H + h, p.H, p.A[h], L, cum);
+    if (tid < Q) ev[tid] = expf(cum[tid]);
+    __syncthreads();
+    const IO *Cg = static_cast<const IO *>(p.C);
+    for (int e = tid; e < Q * N; e += kCT) {
+        const int k = e / N, n = e % N;
+        sCe[e] = k < L ? ev[k] * ldf(Cg, (tok0 + k) * p.G * N + (int64_t)g * N + n) : 0.f;
+    }
+    __syncthreads();
+    const int q = tid % P, n0 = (tid / P) * R;
+    float acc[R];
+#pragma unroll
+    for (int a = 0; a < R; ++a) acc[a] = 0.f;
+#pragma unroll 2
+    for (int k = 0; k < Q; ++k) {
+        const float d = sdY[k * P + q];
+        const float4 *ce = reinterpret_cast<const float4 *>(sCe + k * N + n0);
+#pragma unroll
+        for (int a = 0; a < R / 4; ++a) {
+            const float4 v = ce[a];
+            acc[4 * a] = fmaf(v.x, d, acc[4 * a]);
+            acc[4 * a + 1] = fmaf(v.y, d, acc[4 * a + 1]);
+            acc[4 * a + 2] = fmaf(v.z, d, acc[4 * a + 2]);
+            acc[4 * a + 3] = fmaf(v.w, d, acc[4 * a + 3]);
+        }
+    }
+    float *out = p.gst + (((int64_t)bi * p.H + h) * p.nc + c) * N * P;
+#pragma unroll
+    for (int a = 0; a < R; ++a) out[(int64_t)(n0 + a) * P + q] = acc[a];
+}
+
+// The adjoint chain over chunks, backwards, per (batch row, head, state entry): g starts at
+// dfinal; chunk c's slot receives g (the adjoint at the chunk's end) in place of its r, and
+// g becomes e^{sum of dt A over chunk c} g + r.  What is left at the front is dinit.
+constexpr int kRevU = 4;
+__global__ void __launch_bounds__(kCT) bwd_state_reverse(BwdCParams p) {
+    const int h = blockIdx.y, bi = blockIdx.z;
+    const int64_t NP = (int64_t)p.N * p.P;
+    const int64_t o = (int64_t)blockIdx.x * kCT + threadIdx.x;
+    if (o >= NP) return;
+    const int64_t bh = (int64_t)bi * p.H + h;
+    float g = p.dfinal ? p.dfinal[bh * NP + o] : 0.f;
+    float *gs = p.gst + bh * p.nc * NP + o;
+    const float *cs = p.csum + bh * p.nc;
+    int c = p.nc - 1;
+    for (; c + 1 >= kRevU; c -= kRevU) {
+        float rv[kRevU], cv[kRevU];
+#pragma unroll
+        for (int u = 0; u < kRevU; ++u) {
+            rv[u] = gs[(int64_t)(c - u) * NP];
+            cv[u] = cs[c - u];
+        }
+#pragma unroll
+        for (int u = 0; u < kRevU; ++u) {
+            gs[(int64_t)(c - u) * NP] = g;
+            g = fmaf(expf(cv[u]), g, rv[u]);
+        }
+    }
+    for (; c >= 0; --c) {
+        const float r = gs[(int64_t)c * NP];
+        gs[(int64_t)c * NP] = g;
+        g = fmaf(expf(cs[c]), g, r);
+    }
+    if (p.dinit) p.dinit[bh * NP + o] = g;
+}
+
+// acc[a][j] += sum_k A(m_a, k) Bop(k, n_j) over this thread's outputs m_a = tm + 16 a,
+// n_j = tn + 16 j, with A(m, k) = A[m * am + k * ak] and Bop(k, n) = Bm[k * bk + n * bn].
+// Thread (tm, tn) = (tid / 16, tid % 16): a half warp shares its rows (broadcast loads of A),
+// and its 16 lanes read 16 consecutive columns, or columns an odd stride apart, of Bop
+// (distinct banks: every shared array below has an odd row stride).
+template <int RM, int CN>
+__device__ __forceinline__ void mm(float (&acc)[RM][CN], const float *A, int am, int ak, const float *Bm, int bk,
+                                   int bn, int K, int tm, int tn) {
+#pragma unroll 4
+    for (int k = 0; k < K; ++k) {
+        float av[RM], bv[CN];
+#pragma unroll
+        for (int a = 0; a < RM; ++a) av[a] = A[(tm + 16 * a) * am + k * ak];
+#pragma unroll
+        for (int j = 0; j < CN; ++j) bv[j] = Bm[k * bk + (tn + 16 * j) * bn];
+#pragma unroll
+        for (int a = 0; a < RM; ++a)
+#pragma unroll
+            for (int j = 0; j < CN; ++j) acc[a][j] = fmaf(av[a], bv[j], acc[a][j]);
+    }
+}
+
+template <int RM, int CN> __device__ __forceinline__ void zero(float (&acc)[RM][CN]) {
+#pragma unroll
+    for (int a = 0; a < RM; ++a)
+#pragma unroll
+        for (int j = 0; j < CN; ++j) acc[a][j] = 0.f;
+}
+
+// sum over the 16 lanes of a half warp
+__device__ __forceinline__ float sum16(float v) {
+#pragma unroll
+    for (int o = 8; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+template <int N, int P>
+constexpr size_t chunk_grad_floats() {
+    return 8 + (size_t)2 * kQc * (P + 1) + 2 * kQc * (N + 1) + 2 * N * (P + 1) + 3 * kQc * (kQc + 1) + 5 * kQc;
+}
+
+template <typename IO, int N, int P>
+__global__ void __launch_bounds__(kCT, 1) bwd_chunk_grad(BwdCParams p) {
+    constexpr int Q = kQc, QS = Q + 1, PS = P + 1, NS = N + 1;
+    constexpr int RM = Q / 16, CQ = Q / 16, CP = P / 16, CN = N / 16;
+    extern __shared__ float sm[];
+    double *redd = reinterpret_cast<double *>(sm);   // [2]: <g, h>, dA (8-byte aligned at the start)
+    float *red = sm + 4;              // [2]: dD
+    float *sX = sm + 8;               // [Q][PS]   x
+    float *sdY = sX + Q * PS;         // [Q][PS]   dy
+    float *sB = sdY + Q * PS;         // [Q][NS]   B
+    float *sC = sB + Q * NS;          // [Q][NS]   C
+    float *sH = sC + Q * NS;          // [N][PS]   state entering the chunk
+    float *sGc = sH + N * PS;         // [N][PS]   adjoint at the chunk's end
+    float *sS = sGc + N * PS;         // [Q][QS]   S
+    float *sG = sS + Q * QS;          // [Q][QS]   G
+    float *sK = sG + Q * QS;          // [Q][QS]   K, then its row prefix sums
+    float *cum = sK + Q * QS;         // [Q]
+    float *wv = cum + Q, *ev = wv + Q;
+    float *wvv = ev + Q, *eu = wvv + Q;   // [Q] w_j v_j, e_i u_i
+    const int c = blockIdx.x, h = blockIdx.y, bi = blockIdx.z, tid = threadIdx.x;
+    const int tm = tid >> 4, tn = tid & 15;
+    const int64_t t0 = (int64_t)c * Q;
+    const int L = (int)min((int64_t)Q, (int64_t)p.T - t0);
+    const int g = h / (p.H / p.G);
+    const int64_t bh = (int64_t)bi * p.H + h;
+    const int64_t tok0 = (int64_t)bi * p.T + t0;
+    const float Ah = p.A[h];
+
+    load_rows(sX, PS, static_cast<const IO *>(p.x), tok0 * p.H * P + (int64_t)h * P, (int64_t)p.H * P, Q, L, P);
+    load_rows(sdY, PS, static_cast<const IO *>(p.dy), tok0 * p.H * P + (int64_t)h * P, (int64_t)p.H * P, Q, L, P);
+    load_rows(sB, NS, static_cast<const IO *>(p.B), tok0 * p.G * N + (int64_t)g * N, (int64_t)p.G * N, Q, L, N);
+    load_rows(sC, NS, static_cast<const IO *>(p.C), tok0 * p.G * N + (int64_t)g * N, (int64_t)p.G * N, Q, L, N);
+    {
+        const float4 *hs = reinterpret_cast<const float4 *>(p.states + (bh * p.nc + c) * N * P);
+        const float4 *gs = reinterpret_cast<const float4 *>(p.gst + (bh * p.nc + c) * N * P);
+        for (int e = tid; e < N * P / 4; e += kCT) {
+            const int n = (4 * e) / P, q = (4 * e) % P;
+            const float4 a = hs[e], b = gs[e];
+            float *hd = sH + n * PS + q, *gd = sGc + n * PS + q;
+            hd[0] = a.x; hd[1] = a.y; hd[2] = a.z; hd[3] = a.w;
+            gd[0] = b.x; gd[1] = b.y; gd[2] = b.z; gd[3] = b.w;
+        }
+    }
+    if (tid < 2) {
+        redd[tid] = 0.0;
+        red[tid] = 0.f;
+    }
+    chunk_cum(p.dt + tok0 * p.H + h, p.H, Ah, L, cum);
+    if (tid < Q) {
+        wv[tid] = expf(cum[Q - 1] - cum[tid]);
+        ev[tid] = expf(cum[tid]);
+    }
+    __syncthreads();
+
+    // C B^T and dY X^T; S, G and K = G o (C B^T)
+    {
+        float acb[RM][CQ], ayx[RM][CQ];
+        zero(acb);
+        zero(ayx);
+        mm(acb, sC, NS, 1, sB, 1, NS, N, tm, tn);
+        mm(ayx, sdY, PS, 1, sX, 1, PS, P, tm, tn);
+#pragma unroll
+        for (int a = 0; a < RM; ++a) {
+            const int i = tm + 16 * a;
+#pragma unroll
+            for (int j = 0; j < CQ; ++j) {
+                const int jj = tn + 16 * j;
+                float sv = 0.f, gv = 0.f;
+                if (jj <= i) {
+                    const float l = expf(cum[i] - cum[jj]);
+                    sv = l * acb[a][j];
+                    gv = l * ayx[a][j];
+                }
+                sS[i * QS + jj] = sv;
+                sG[i * QS + jj] = gv;
+                sK[i * QS + jj] = gv * acb[a][j];
+            }
+        }
+    }
+    __syncthreads();
+
+    // dX = S^T dY + w o (B g) + D dY;  v_j = x_j.(B g)_j;  dD
+    {
+        float asd[RM][CP], abg[RM][CP];
+        zero(asd);
+        zero(abg);
+        mm(asd, sS, 1, QS, sdY, PS, 1, Q, tm, tn);
+        mm(abg, sB, NS, 1, sGc, PS, 1, N, tm, tn);
+        const float Dh = p.D ? p.D[h] : 0.f;
+        IO *dx = static_cast<IO *>(p.dx);
+        float dd = 0.f;
+#pragma unroll
+        for (int a = 0; a < RM; ++a) {
+            const int j = tm + 16 * a;
+            float vj = 0.f;
+#pragma unroll
+            for (int k = 0; k < CP; ++k) {
+                const int q = tn + 16 * k;
+                const float xv = sX[j * PS + q], dyv = sdY[j * PS + q];
+                vj = fmaf(abg[a][k], xv, vj);
+                dd = fmaf(dyv, xv, dd);
+                if (j < L) stf(dx, (tok0 + j) * p.H * P + (int64_t)h * P + q, fmaf(wv[j], abg[a][k], fmaf(Dh, dyv, asd[a][k])));
+            }
+            vj = sum16(vj);
+            if (tn == 0) wvv[j] = wv[j] * vj;
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) dd += __shfl_xor_sync(0xffffffffu, dd, o);
+        if ((tid & 31) == 0) atomicAdd(red + 0, dd);
+    }
+
+    // dC = G B + e o (dY h^T);  u_i = C_i.(h dY_i)
+    {
+        float agb[RM][CN], ayh[RM][CN];
+        zero(agb);
+        zero(ayh);
+        mm(agb, sG, QS, 1, sB, NS, 1, Q, tm, tn);
+        mm(ayh, sdY, PS, 1, sH, 1, PS, P, tm, tn);
+#pragma unroll
+        for (int a = 0; a < RM; ++a) {
+            const int i = tm + 16 * a;
+            float ui = 0.f;
+#pragma unroll
+            for (int k = 0; k < CN; ++k) {
+                const int n = tn + 16 * k;
+                ui = fmaf(sC[i * NS + n], ayh[a][k], ui);
+                if (i < L) p.dCh[((tok0 + i) * p.H + h) * N + n] = fmaf(ev[i], ayh[a][k], agb[a][k]);
+            }
+            ui = sum16(ui);
+            if (tn == 0) eu[i] = ev[i] * ui;
+        }
+    }
+
+    // dB = G^T C + w o (X g^T)
+    {
+        float agc[RM][CN], axg[RM][CN];
+        zero(agc);
+        zero(axg);
+        mm(agc, sG, 1, QS, sC, NS, 1, Q, tm, tn);
+        mm(axg, sX, PS, 1, sGc, 1, PS, P, tm, tn);
+#pragma unroll
+        for (int a = 0; a < RM; ++a) {
+            const int j = tm + 16 * a;
+            if (j < L) {
+#pragma unroll
+                for (int k = 0; k < CN; ++k)
+                    p.dBh[((tok0 + j) * p.H + h) * N + tn + 16 * k] = fmaf(wv[j], axg[a][k], agc[a][k]);
+            }
+        }
+    }
+
+    // <g, h> (fp32 per thread, double across threads); row prefix sums of K (exclusive)
+    {
+        float gh = 0.f;
+        for (int e = tid; e < N * P; e += kCT) {
+            const int n = e / P, q = e % P;
+            gh = fmaf(sGc[n * PS + q], sH[n * PS + q], gh);
+        }
+        double ghd = gh;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) ghd += __shfl_xor_sync(0xffffffffu, ghd, o);
+        if ((tid & 31) == 0) atomicAdd(redd + 0, ghd);
+        if (tid < Q) {
+            float acc = 0.f;
+            for (int j = 0; j < Q; ++j) {
+                const float kv = sK[tid * QS + j];
+                sK[tid * QS + j] = acc;
+                acc += kv;
+            }
+        }
+    }
+    __syncthreads();
+
+    // rc_k (double), ddt, dA and dD
+    if (tid < Q) {
+        const int k = tid;
+        double rc = exp((double)cum[Q - 1]) * redd[0];
+        for (int j = 0; j < k; ++j) rc += (double)wvv[j];
+        for (int i = k; i < Q; ++i) rc += (double)sK[i * QS + k] + (double)eu[i];
+        double da = 0.0;
+        if (k < L) {
+            const int64_t o = (tok0 + k) * p.H + h;
+            p.ddt[o] = (float)(Ah * rc);
+            da = (double)p.dt[o] * rc;
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) da += __shfl_xor_sync(0xffffffffu, da, o);
+        if ((tid & 31) == 0) atomicAdd(redd + 1, da);
+    }
+    __syncthreads();
+    if (tid == 0) {
+        atomicAdd(p.dA + h, (float)redd[1]);
+        if (p.dD) atomicAdd(p.dD + h, red[0]);
+    }
+}
+
 struct BwdLayout {
     int R, nsl, nK;
     size_t off_ck, off_dbh, off_dch, off_dl, off_dxa, total;
@@ -370,6 +757,95 @@ cudaError_t launch_all(const Problem &p, const BwdParams &bp, const BwdLayout &l
     return cudaGetLastError();
 }
 
+// ---- chunked path: host side ----
+// the chunked path's domain: scalar A at the head dims its kernels are built for
+bool chunked_applies(const Problem &p) {
+    if (p.a_mode != SSD_A_SCALAR || p.P != 64 || (p.N != 64 && p.N != 128)) return false;
+    if (p.H > 65535 || p.b > 65535 || (p.T + kQc - 1) / kQc > (int64_t)INT32_MAX) return false;
+    Problem q = p;
+    q.Q = kQc;
+    q.nc = (p.T + kQc - 1) / kQc;
+    return generic_supports(q);
+}
+
+struct BwdCLayout {
+    int64_t nc;
+    size_t off_cs, off_st, off_g, off_dbh, off_dch, total;
+};
+
+BwdCLayout bwdc_layout(const Problem &p) {
+    BwdCLayout l;
+    l.nc = (p.T + kQc - 1) / kQc;
+    const size_t tokh = (size_t)(p.b * p.T * p.H), np = (size_t)(p.b * p.H * l.nc * p.N * p.P);
+    l.off_cs = kStatusBytes;
+    l.off_st = align_up(l.off_cs + sizeof(float) * (size_t)(p.b * p.H * l.nc), 256);
+    l.off_g = align_up(l.off_st + sizeof(float) * np, 256);
+    l.off_dbh = align_up(l.off_g + sizeof(float) * np, 256);
+    l.off_dch = align_up(l.off_dbh + sizeof(float) * tokh * p.N, 256);
+    l.total = align_up(l.off_dch + sizeof(float) * tokh * p.N, 256);
+    return l;
+}
+
+template <typename IO, int N>
+cudaError_t launch_chunked_typed(const Problem &p, const BwdCParams &cp, cudaStream_t s) {
+    constexpr int P = 64;
+    const size_t sm_r = sizeof(float) * (size_t)(kQc * N + kQc * P + 2 * kQc);
+    const size_t sm_g = sizeof(float) * chunk_grad_floats<N, P>();
+    cudaError_t e = cudaFuncSetAttribute(bwd_chunk_r<IO, N, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_r);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(bwd_chunk_grad<IO, N, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_g);
+    if (e != cudaSuccess) return e;
+    const dim3 grid((unsigned)cp.nc, (unsigned)p.H, (unsigned)p.b);
+    bwd_chunk_r<IO, N, P><<<grid, kCT, sm_r, s>>>(cp);
+    bwd_state_reverse<<<dim3((unsigned)((N * P + kCT - 1) / kCT), (unsigned)p.H, (unsigned)p.b), kCT, 0, s>>>(cp);
+    record_dominant_start(s);
+    bwd_chunk_grad<IO, N, P><<<grid, kCT, sm_g, s>>>(cp);
+    record_dominant_stop(s);
+    note_launches(3);
+    return cudaGetLastError();
+}
+
+cudaError_t chunked_launch(const Problem &p, const BwdGrads &gr, char *base, cudaStream_t s) {
+    const BwdCLayout l = bwdc_layout(p);
+    // the state entering every chunk: the generic forward's chunk-state and state-passing kernels
+    Problem q = p;
+    q.Q = kQc;
+    q.nc = l.nc;
+    q.y = nullptr;
+    q.final_state = nullptr;
+    GenericWorkspace gw;
+    gw.status = reinterpret_cast<int *>(base);
+    gw.chunk_sum = reinterpret_cast<float *>(base + l.off_cs);
+    gw.states = reinterpret_cast<float *>(base + l.off_st);
+    cudaError_t e = generic_states_launch(q, gw, s);
+    if (e != cudaSuccess) return e;
+    BwdCParams cp;
+    cp.x = p.x; cp.B = p.B; cp.C = p.C; cp.dy = gr.dy;
+    cp.dt = p.dt; cp.A = p.A; cp.D = p.D; cp.dfinal = gr.dfinal;
+    cp.dx = gr.dx; cp.ddt = gr.ddt; cp.dA = gr.dA; cp.dD = gr.dD; cp.dinit = gr.dinit;
+    cp.states = gw.states;
+    cp.csum = gw.chunk_sum;
+    cp.gst = reinterpret_cast<float *>(base + l.off_g);
+    cp.dBh = reinterpret_cast<float *>(base + l.off_dbh);
+    cp.dCh = reinterpret_cast<float *>(base + l.off_dch);
+    cp.b = (int)p.b; cp.T = (int)p.T; cp.H = (int)p.H; cp.G = (int)p.G; cp.N = (int)p.N; cp.P = (int)p.P;
+    cp.nc = (int)l.nc;
+    const bool bf = p.io_dtype == SSD_DTYPE_BF16;
+    if (p.N == 64) e = bf ? launch_chunked_typed<__nv_bfloat16, 64>(p, cp, s) : launch_chunked_typed<float, 64>(p, cp, s);
+    else e = bf ? launch_chunked_typed<__nv_bfloat16, 128>(p, cp, s) : launch_chunked_typed<float, 128>(p, cp, s);
+    if (e != cudaSuccess) return e;
+    // dB, dC: the per-head sums over each group's heads
+    BwdParams bp;
+    std::memset(&bp, 0, sizeof(bp));
+    bp.dB = gr.dB; bp.dC = gr.dC;
+    bp.dBh = cp.dBh; bp.dCh = cp.dCh;
+    bp.b = (int)p.b; bp.T = (int)p.T; bp.H = (int)p.H; bp.N = (int)p.N; bp.G = (int)p.G;
+    if (bf) bwd_finish_bc<__nv_bfloat16><<<1184, 256, 0, s>>>(bp);
+    else bwd_finish_bc<float><<<1184, 256, 0, s>>>(bp);
+    note_launches(1);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 bool bwd_supports(const Problem &p) {
@@ -380,11 +856,20 @@ bool bwd_supports(const Problem &p) {
     return true;
 }
 
-size_t bwd_workspace_bytes(const Problem &p) { return bwd_layout(p).total; }
+size_t bwd_workspace_bytes(const Problem &p) {
+    return chunked_applies(p) ? bwdc_layout(p).total : bwd_layout(p).total;
+}
 
 cudaError_t bwd_launch(const Problem &p, const BwdGrads &gr, void *ws, cudaStream_t s) {
-    const BwdLayout l = bwd_layout(p);
     char *base = static_cast<char *>(ws);
+    if (chunked_applies(p)) {
+        cudaError_t e = cudaMemsetAsync(base, 0, kStatusBytes, s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(gr.dA, 0, sizeof(float) * (size_t)p.H, s);
+        if (e == cudaSuccess && gr.dD) e = cudaMemsetAsync(gr.dD, 0, sizeof(float) * (size_t)p.H, s);
+        if (e != cudaSuccess) return e;
+        return chunked_launch(p, gr, base, s);
+    }
+    const BwdLayout l = bwd_layout(p);
     BwdParams bp;
     bp.x = p.x; bp.B = p.B; bp.C = p.C; bp.dy = gr.dy;
     bp.dt = p.dt; bp.A = p.A; bp.D = p.D; bp.init = p.init; bp.dfinal = gr.dfinal;

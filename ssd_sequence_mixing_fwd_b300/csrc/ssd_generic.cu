@@ -416,13 +416,10 @@ cudaError_t launch_state(const Problem &p, const GenericWorkspace &w, cudaStream
     return cudaGetLastError();
 }
 
+// The first two kernels: chunk states, then the states entering every chunk (in place).
 template <typename IO>
-cudaError_t launch_typed(const Problem &p, const GenericWorkspace &w, cudaStream_t s) {
-    const size_t sm3 = output_smem(p);
+cudaError_t launch_states(const Problem &p, const GenericWorkspace &w, cudaStream_t s) {
     cudaError_t e;
-    if ((e = cudaFuncSetAttribute(gen_chunk_output<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)sm3)) != cudaSuccess)
-        return e;
     // accumulators per thread of the chunk-state kernel: N / (threads / P), rounded up
     const int64_t nacc = (p.N + (kThreads / p.P) - 1) / (kThreads / p.P);
     if (nacc <= 4) e = launch_state<IO, 4>(p, w, s);
@@ -433,7 +430,17 @@ cudaError_t launch_typed(const Problem &p, const GenericWorkspace &w, cudaStream
     if (e != cudaSuccess) return e;
     dim3 g2((unsigned)((p.N * p.P + kThreads - 1) / kThreads), (unsigned)p.H, (unsigned)p.b);
     gen_state_passing<<<g2, kThreads, 0, s>>>(p, w);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+template <typename IO>
+cudaError_t launch_typed(const Problem &p, const GenericWorkspace &w, cudaStream_t s) {
+    const size_t sm3 = output_smem(p);
+    cudaError_t e;
+    if ((e = cudaFuncSetAttribute(gen_chunk_output<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)sm3)) != cudaSuccess)
+        return e;
+    if ((e = launch_states<IO>(p, w, s)) != cudaSuccess) return e;
     const int64_t nrt = (p.Q + kRT - 1) / kRT;
     dim3 g3((unsigned)(p.nc * nrt), (unsigned)p.H, (unsigned)p.b);
     record_dominant_start(s);
@@ -476,6 +483,12 @@ GenericWorkspace generic_carve(const Problem &p, void *ws) {
 cudaError_t generic_launch(const Problem &p, const GenericWorkspace &w, cudaStream_t s) {
     if (p.io_dtype == SSD_DTYPE_BF16) return launch_typed<__nv_bfloat16>(p, w, s);
     return launch_typed<float>(p, w, s);
+}
+
+cudaError_t generic_states_launch(const Problem &p, const GenericWorkspace &w, cudaStream_t s) {
+    cudaError_t e = p.io_dtype == SSD_DTYPE_BF16 ? launch_states<__nv_bfloat16>(p, w, s) : launch_states<float>(p, w, s);
+    if (e == cudaSuccess) note_launches(2);
+    return e;
 }
 
 }  // namespace ssd

@@ -5,9 +5,10 @@ tensor (relative L2).  Tolerances: fp32 io 1e-5 (fp32 arithmetic throughout);
 bf16 io 2e-3 (dx, dB and dC are rounded to bf16 on output; the fp32 outputs
 ddt, dA, dD and dinit are held to 1e-4).  Cases cover both A modes, D and the
 initial state present or absent, dfinal present or absent, several B/C
-groups, ragged lengths around the 32-token checkpoint block, a state
-dimension that does not fill its last slice of rows, and the head dims the
-kernel takes.
+groups, ragged lengths around the 8-token checkpoint blocks of the recurrence
+path and the 64-token chunks of the chunked path (scalar A at P 64, N 64 or
+128), a state dimension that does not fill its last slice of rows, and the
+head dims each path takes.
 """
 import numpy as np
 import pytest
@@ -72,6 +73,16 @@ CASES = [
     ("scalar_f32_P4_T1", Workload("t", b=3, T=1, H=2, P=4, N=8, G=1, Q=64, dtype="f32", D="normal",
                                   init_std=0.5, seed=706)),
     ("scalar_bf16_T32", Workload("t", b=1, T=32, H=2, P=64, N=128, G=1, Q=128, D="none", seed=707)),
+    # the chunked path (scalar A, P 64, N 64 or 128): 64-token chunks, ragged tails, one-token
+    # sequences, fp32 io at 1e-5, two B/C groups
+    ("chunked_f32_N64_G2", Workload("t", b=2, T=150, H=4, P=64, N=64, G=2, Q=64, dtype="f32", D="normal",
+                                    init_std=0.2, seed=721)),
+    ("chunked_f32_N128_T65", Workload("t", b=1, T=65, H=2, P=64, N=128, G=1, Q=128, dtype="f32", D="ones",
+                                      init_std=0.3, seed=722)),
+    ("chunked_bf16_N64_T1", Workload("t", b=3, T=1, H=2, P=64, N=64, G=1, Q=64, D="normal", init_std=0.5,
+                                     seed=723)),
+    ("chunked_bf16_N128_G2_T200", Workload("t", b=2, T=200, H=6, P=64, N=128, G=2, Q=256, D="none",
+                                           init_std=0.1, seed=724)),
 ]
 
 
