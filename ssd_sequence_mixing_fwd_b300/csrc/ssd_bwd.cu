@@ -376,13 +376,48 @@ __device__ __forceinline__ void chunk_cum(const float *dt, int64_t stride, float
     __syncthreads();
 }
 
-// dst[k * ds + c] = src[base + k * rs + c] (fp32) for k < valid, 0 for valid <= k < rows.
-template <typename IO>
-__device__ __forceinline__ void load_rows(float *dst, int ds, const IO *src, int64_t base, int64_t rs, int rows,
-                                          int valid, int cols) {
-    for (int e = threadIdx.x; e < rows * cols; e += blockDim.x) {
-        const int k = e / cols, c = e % cols;
-        dst[k * ds + c] = k < valid ? ldf(src, base + k * rs + c) : 0.f;
+// 16 bytes of io values as fp32
+__device__ __forceinline__ void unpack16(const uint4 &u, const float *, float (&f)[4]) {
+    f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y); f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
+}
+__device__ __forceinline__ void unpack16(const uint4 &u, const __nv_bfloat16 *, float (&f)[8]) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
+// dst[k * ds + c] = scale_k * src[base + k * rs + c] (fp32) for k < valid, 0 past valid, over a
+// ROWS x COLS tile: every thread issues all of its 16-byte loads before its first store (the
+// rows start on 16-byte boundaries: COLS, rs and base are multiples of the 16-byte vector)
+template <typename IO, int ROWS, int COLS>
+__device__ __forceinline__ void load_tile(float *dst, int ds, const IO *src, int64_t base, int64_t rs, int valid,
+                                          const float *scale = nullptr) {
+    constexpr int V = 16 / sizeof(IO);
+    constexpr int NV = ROWS * COLS / V;
+    constexpr int PER = (NV + kCT - 1) / kCT;
+    static_assert(COLS % V == 0, "tile rows are whole 16-byte vectors");
+    uint4 buf[PER];
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+        const int e = threadIdx.x + u * kCT;
+        const int k = (e * V) / COLS, c = (e * V) % COLS;
+        buf[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (e < NV && k < valid) buf[u] = __ldg(reinterpret_cast<const uint4 *>(src + base + (int64_t)k * rs + c));
+    }
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+        const int e = threadIdx.x + u * kCT;
+        if (e < NV) {
+            const int k = (e * V) / COLS, c = (e * V) % COLS;
+            float f[V];
+            unpack16(buf[u], src, f);
+            const float sc = scale ? scale[k] : 1.f;
+#pragma unroll
+            for (int v = 0; v < V; ++v) dst[k * ds + c + v] = sc * f[v];
+        }
     }
 }
 
@@ -401,15 +436,11 @@ __global__ void __launch_bounds__(kCT) bwd_chunk_r(BwdCParams p) {
     const int L = (int)min((int64_t)Q, (int64_t)p.T - t0);
     const int g = h / (p.H / p.G);
     const int64_t tok0 = (int64_t)bi * p.T + t0;
-    load_rows(sdY, P, static_cast<const IO *>(p.dy), tok0 * p.H * P + (int64_t)h * P, (int64_t)p.H * P, Q, L, P);
+    load_tile<IO, Q, P>(sdY, P, static_cast<const IO *>(p.dy), tok0 * p.H * P + (int64_t)h * P, (int64_t)p.H * P, L);
     chunk_cum(p.dt + tok0 * p.H + h, p.H, p.A[h], L, cum);
     if (tid < Q) ev[tid] = expf(cum[tid]);
     __syncthreads();
-    const IO *Cg = static_cast<const IO *>(p.C);
-    for (int e = tid; e < Q * N; e += kCT) {
-        const int k = e / N, n = e % N;
-        sCe[e] = k < L ? ev[k] * ldf(Cg, (tok0 + k) * p.G * N + (int64_t)g * N + n) : 0.f;
-    }
+    load_tile<IO, Q, N>(sCe, N, static_cast<const IO *>(p.C), tok0 * p.G * N + (int64_t)g * N, (int64_t)p.G * N, L, ev);
     __syncthreads();
     const int q = tid % P, n0 = (tid / P) * R;
     float acc[R];
@@ -436,7 +467,7 @@ __global__ void __launch_bounds__(kCT) bwd_chunk_r(BwdCParams p) {
 // The adjoint chain over chunks, backwards, per (batch row, head, state entry): g starts at
 // dfinal; chunk c's slot receives g (the adjoint at the chunk's end) in place of its r, and
 // g becomes e^{sum of dt A over chunk c} g + r.  What is left at the front is dinit.
-constexpr int kRevU = 4;
+constexpr int kRevU = 16;
 __global__ void __launch_bounds__(kCT) bwd_state_reverse(BwdCParams p) {
     const int h = blockIdx.y, bi = blockIdx.z;
     const int64_t NP = (int64_t)p.N * p.P;
@@ -537,21 +568,12 @@ __global__ void __launch_bounds__(kCT, 1) bwd_chunk_grad(BwdCParams p) {
     const int64_t tok0 = (int64_t)bi * p.T + t0;
     const float Ah = p.A[h];
 
-    load_rows(sX, PS, static_cast<const IO *>(p.x), tok0 * p.H * P + (int64_t)h * P, (int64_t)p.H * P, Q, L, P);
-    load_rows(sdY, PS, static_cast<const IO *>(p.dy), tok0 * p.H * P + (int64_t)h * P, (int64_t)p.H * P, Q, L, P);
-    load_rows(sB, NS, static_cast<const IO *>(p.B), tok0 * p.G * N + (int64_t)g * N, (int64_t)p.G * N, Q, L, N);
-    load_rows(sC, NS, static_cast<const IO *>(p.C), tok0 * p.G * N + (int64_t)g * N, (int64_t)p.G * N, Q, L, N);
-    {
-        const float4 *hs = reinterpret_cast<const float4 *>(p.states + (bh * p.nc + c) * N * P);
-        const float4 *gs = reinterpret_cast<const float4 *>(p.gst + (bh * p.nc + c) * N * P);
-        for (int e = tid; e < N * P / 4; e += kCT) {
-            const int n = (4 * e) / P, q = (4 * e) % P;
-            const float4 a = hs[e], b = gs[e];
-            float *hd = sH + n * PS + q, *gd = sGc + n * PS + q;
-            hd[0] = a.x; hd[1] = a.y; hd[2] = a.z; hd[3] = a.w;
-            gd[0] = b.x; gd[1] = b.y; gd[2] = b.z; gd[3] = b.w;
-        }
-    }
+    load_tile<IO, Q, P>(sX, PS, static_cast<const IO *>(p.x), tok0 * p.H * P + (int64_t)h * P, (int64_t)p.H * P, L);
+    load_tile<IO, Q, P>(sdY, PS, static_cast<const IO *>(p.dy), tok0 * p.H * P + (int64_t)h * P, (int64_t)p.H * P, L);
+    load_tile<IO, Q, N>(sB, NS, static_cast<const IO *>(p.B), tok0 * p.G * N + (int64_t)g * N, (int64_t)p.G * N, L);
+    load_tile<IO, Q, N>(sC, NS, static_cast<const IO *>(p.C), tok0 * p.G * N + (int64_t)g * N, (int64_t)p.G * N, L);
+    load_tile<float, N, P>(sH, PS, p.states, (bh * p.nc + c) * N * P, P, N);
+    load_tile<float, N, P>(sGc, PS, p.gst, (bh * p.nc + c) * N * P, P, N);
     if (tid < 2) {
         redd[tid] = 0.0;
         red[tid] = 0.f;

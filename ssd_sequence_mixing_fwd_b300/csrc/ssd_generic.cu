@@ -32,7 +32,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kTT = 16;        // tokens per shared-memory tile (chunk state)
 constexpr int kMaxAcc = 64;    // N*P / 256 accumulators per thread at most (chunk state)
-constexpr int kPassU = 8;      // chunks whose states are loaded together (state passing)
+constexpr int kPassU = 16;     // chunks whose states are loaded together (state passing)
 constexpr int kRT = 32;        // output rows per block
 constexpr int kJT = 32;        // key (j) columns per tile
 constexpr int kMaxOut = 32;    // kRT*P / 256 outputs per thread at most
