@@ -507,7 +507,7 @@ __global__ void __launch_bounds__(kCT) bwd_state_reverse(BwdCParams p) {
 template <int RM, int CN>
 __device__ __forceinline__ void mm(float (&acc)[RM][CN], const float *A, int am, int ak, const float *Bm, int bk,
                                    int bn, int K, int tm, int tn) {
-#pragma unroll 4
+#pragma unroll 8
     for (int k = 0; k < K; ++k) {
         float av[RM], bv[CN];
 #pragma unroll
@@ -693,25 +693,46 @@ __global__ void __launch_bounds__(kCT, 1) bwd_chunk_grad(BwdCParams p) {
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) ghd += __shfl_xor_sync(0xffffffffu, ghd, o);
         if ((tid & 31) == 0) atomicAdd(redd + 0, ghd);
-        if (tid < Q) {
-            float acc = 0.f;
-            for (int j = 0; j < Q; ++j) {
-                const float kv = sK[tid * QS + j];
-                sK[tid * QS + j] = acc;
-                acc += kv;
-            }
+        // exclusive prefix sums along each row of K: four threads per row, 16 entries each
+        static_assert(Q * 4 == kCT, "four threads per row of K");
+        const int i = tid >> 2, part = tid & 3;
+        float loc[Q / 4];
+        float run = 0.f;
+#pragma unroll
+        for (int jj = 0; jj < Q / 4; ++jj) {
+            loc[jj] = run;
+            run += sK[i * QS + part * (Q / 4) + jj];
         }
+        float v = run;
+#pragma unroll
+        for (int o = 1; o < 4; o <<= 1) {
+            const float u = __shfl_up_sync(0xffffffffu, v, o, 4);
+            if (part >= o) v += u;
+        }
+        const float off = v - run;
+#pragma unroll
+        for (int jj = 0; jj < Q / 4; ++jj) sK[i * QS + part * (Q / 4) + jj] = loc[jj] + off;
     }
     __syncthreads();
 
-    // rc_k (double), ddt, dA and dD
-    if (tid < Q) {
-        const int k = tid;
-        double rc = exp((double)cum[Q - 1]) * redd[0];
-        for (int j = 0; j < k; ++j) rc += (double)wvv[j];
-        for (int i = k; i < Q; ++i) rc += (double)sK[i * QS + k] + (double)eu[i];
+    // rc_k, four threads per token (fp32 partial sums, combined in double); ddt, dA and dD
+    {
+        const int k = tid >> 2, part = tid & 3;
+        float cs = 0.f, es = 0.f, ws = 0.f;
+        for (int ii = part; ii < Q; ii += 4) {
+            if (ii >= k) {
+                cs += sK[ii * QS + k];
+                es += eu[ii];
+            } else {
+                ws += wvv[ii];
+            }
+        }
+        double rc = (double)cs + (double)es + (double)ws;
+        rc += __shfl_xor_sync(0xffffffffu, rc, 1);
+        rc += __shfl_xor_sync(0xffffffffu, rc, 2);
+        rc += exp((double)cum[Q - 1]) * redd[0];
         double da = 0.0;
-        if (k < L) {
+        if (part == 0 && k < L) {
             const int64_t o = (tok0 + k) * p.H + h;
             p.ddt[o] = (float)(Ah * rc);
             da = (double)p.dt[o] * rc;
