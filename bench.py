@@ -145,7 +145,8 @@ def time_backward(ssd, torch, w, d, dev, stream, flush, peaks, args):
     """ssd_bwd on the bench inputs: the whole call (checkpoints, reverse sweep, finishing kernels),
     CUDA events on the launching stream, L2 flushed before each call; plus the fp64 backward
     oracle on a bounded sample of the same workload on the host cores."""
-    from ssd_sequence_mixing_fwd_b300.inputs import algorithmic_bytes_bwd, make_inputs
+    from ssd_sequence_mixing_fwd_b300.inputs import (algorithmic_bytes_bwd, algorithmic_flops_bwd,
+                                                     bwd_chunked_applies, make_inputs)
     g = torch.Generator(device="cpu").manual_seed(4242)
     dy = torch.randn(d["x"].shape, generator=g).to(d["x"].dtype).to(dev)
     b, T, H, P = d["x"].shape
@@ -168,12 +169,26 @@ def time_backward(ssd, torch, w, d, dev, stream, flush, peaks, args):
                 times.append(e0.elapsed_time(e1))
     ms = sum(times) / len(times)
     by = algorithmic_bytes_bwd(w)
-    ent = {"path": "generic (CUDA cores)", "call_ms": ms, "tokens_per_s": w.tokens / (ms / 1e3),
+    chunked = bwd_chunked_applies(w)
+    ent = {"path": ("chunked: 64-token chunks, fp32 products on the CUDA cores" if chunked
+                    else "token recurrence on the CUDA cores"),
+           "call_ms": ms, "tokens_per_s": w.tokens / (ms / 1e3),
            "workspace_bytes": ws.numel(),
            "roofline": {"bound": "hbm", "achieved": by / (ms / 1e3) / 1e9, "peak": peaks["hbm_gbs"],
                         "unit": "GB/s", "frac": by / (ms / 1e3) / 1e9 / peaks["hbm_gbs"], "algorithmic_bytes": by},
-           "note": "3 calls after 1 warm-up; the call includes the checkpoint sweep, the reverse sweep, "
-                   "the finishing kernels and the workspace clears"}
+           "note": "3 calls after 1 warm-up; the call includes every kernel of the pass and the "
+                   "workspace clears"}
+    if chunked:
+        # the chunked backward runs its products in exact fp32 on the CUDA cores: the FP32 FMA
+        # peak (SMs x 128 FMA lanes x 2 FLOP x the maximum SM clock) is the ceiling of that design
+        fl = algorithmic_flops_bwd(w)
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        mhz = args.sm_max_mhz if getattr(args, "sm_max_mhz", None) else 2032.0
+        peak = sms * 128 * 2 * mhz * 1e6 / 1e12
+        ent["roofline_alu"] = {"bound": "alu", "achieved": fl / (ms / 1e3) / 1e12, "peak": peak,
+                               "unit": "TFLOP/s", "frac": fl / (ms / 1e3) / 1e12 / peak,
+                               "algorithmic_flops": fl,
+                               "peak_note": "%d SMs x 128 FP32 FMA lanes x 2 x %.0f MHz" % (sms, mhz)}
     if not args.no_cpu_baseline:
         import time as _time
         import oracle
@@ -518,7 +533,9 @@ def run_ours(args, w):
                                       "chunked_speedup = linear-form time / chunked kernel time; the oracle "
                                       "(cpu_baseline) is this same recurrence in fp64"}
         out["decode_step"] = time_decode(ssd, torch, w, d, dev, stream, peaks)
-        # the backward pass (ssd_bwd, CUDA cores) on the same inputs with random cotangents
+        # the backward pass (ssd_bwd, CUDA cores) on the same inputs with random cotangents; its ALU
+        # ceiling takes the maximum SM clock nvidia-smi reported for the timed region
+        args.sm_max_mhz = (out.get("clocks") or {}).get("sm_max_mhz")
         out["backward"] = time_backward(ssd, torch, w, d, dev, stream, flush, peaks, args)
         # the other workloads the parity targets are quoted on, timed in the same run: kernel time,
         # roofline fraction, path, and the oracle on a bounded sample of each

@@ -210,9 +210,16 @@ SSD_API int ssd_decode_step(const ssd_dims *dims,
  * what Structured State Space Duality, "The chunked algorithm takes both",
  * weighs; the pages give no backward, so this is the chain rule of the
  * recurrence of "The recurrence as one matrix").  CUDA cores, fp32
- * arithmetic: a forward sweep stores the state at the start of every
- * 8-token block, and a reverse sweep recomputes each block's states from it
- * while it runs the adjoint recurrence g = C_t dy_t^T + a_{t+1} (.) g.
+ * arithmetic, two paths:
+ *  - scalar A with P == 64 and N in {64, 128}: the chunked algorithm run
+ *    backwards on 64-token chunks -- the state entering every chunk (the
+ *    generic forward's chunk-state kernels), the adjoint at every chunk's
+ *    end (a reverse scan over chunks), then per chunk and head the dense
+ *    products of the quadratic form and the rank-N terms;
+ *  - every other dims: a forward sweep stores the state at the start of
+ *    every 8-token block, and a reverse sweep recomputes each block's states
+ *    from it while it runs the adjoint recurrence
+ *    g = C_t dy_t^T + a_{t+1} (.) g.
  *
  * Inputs (device memory, layouts of ssd_fwd): x, dt, A, B, C, D (or NULL),
  * init_state (or NULL) as given to the forward call; dy (b,T,H,P) io dtype;
@@ -225,8 +232,11 @@ SSD_API int ssd_decode_step(const ssd_dims *dims,
  * dims->path must be SSD_PATH_AUTO or SSD_PATH_GENERIC (SSD_ERR_UNSUPPORTED
  * otherwise); the backward takes 4 <= P <= 128.  Every pointer 16-byte
  * aligned; workspace >= ssd_bwd_workspace_size bytes, 256-byte aligned
- * (checkpoints b*H*ceil(N/(1024/P))*ceil(T/8)*4 KB plus fp32 per-token
- * arrays of 3*b*T*H*N + b*T*H*P floats).  Asynchronous on `stream`; on any
+ * (chunked path: two fp32 arrays of b*H*ceil(T/64)*N*P floats -- the states
+ * and the adjoints -- plus 2*b*T*H*N floats of per-head dB and dC; the
+ * other path: checkpoints b*H*ceil(N/(1024/P))*ceil(T/8)*4 KB plus fp32
+ * per-token arrays of 3*b*T*H*N + b*T*H*P floats; each region rounded up to
+ * 256 bytes).  Asynchronous on `stream`; on any
  * argument error nothing is enqueued.  b == 0 or T == 0: dA and dD are zero
  * and dinit is dfinal (or zero). */
 SSD_API int ssd_bwd_workspace_size(const ssd_dims *dims, size_t *bytes);

@@ -125,6 +125,21 @@ def algorithmic_bytes_bwd(w: Workload) -> int:
     return by
 
 
+def bwd_chunked_applies(w: Workload) -> bool:
+    """Whether ssd_bwd takes its chunked path (scalar A, P 64, N 64 or 128) for ``w``."""
+    return w.a_mode == "scalar" and w.P == 64 and w.N in (64, 128)
+
+
+def algorithmic_flops_bwd(w: Workload, Q: int = 64) -> float:
+    """Causal work of the chunked backward on Q-token chunks (every product a multiply-add
+    pair): per chunk and head, C B^T, dY X^T, S^T dY, G B and G^T C on the causal triangle
+    (1.5 Q^2 N + Q^2 P) and the five rank-N products B g, dY h^T, X g^T, C^T (e o dY) and
+    the chunk state B^T (w o X) (5 Q N P)."""
+    nc = -(-w.T // Q)
+    per = 1.5 * Q * Q * w.N + Q * Q * w.P + 5 * Q * w.N * w.P
+    return 2.0 * per * w.b * w.H * nc
+
+
 def algorithmic_flops(w: Workload) -> float:
     """Causal tensor-core work of the chunked algorithm (elementwise work excluded).
 
