@@ -510,7 +510,7 @@ def run_ours(args, w):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = oracle_sample(w, host, args.cpu_budget)
-    if rank == 0 and world == 1 and not args.no_secondary:
+    if rank == 0 and world == 1 and not args.no_extras:
         # the linear form (ssd_scan: the recurrence token by token on CUDA cores) on the same
         # inputs: the comparison the pages draw between the two forms (context, not a target)
         lin = []
@@ -537,6 +537,7 @@ def run_ours(args, w):
         # ceiling takes the maximum SM clock nvidia-smi reported for the timed region
         args.sm_max_mhz = (out.get("clocks") or {}).get("sm_max_mhz")
         out["backward"] = time_backward(ssd, torch, w, d, dev, stream, flush, peaks, args)
+    if rank == 0 and world == 1 and not args.no_secondary:
         # the other workloads the parity targets are quoted on, timed in the same run: kernel time,
         # roofline fraction, path, and the oracle on a bounded sample of each
         from ssd_sequence_mixing_fwd_b300.inputs import WORKLOAD_ORDER, WORKLOADS
@@ -611,6 +612,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip timing the other workloads (the `secondary` key)")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the linear form, the decode step and the backward pass")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch size (small cases for profiler captures)")
