@@ -339,10 +339,11 @@ __global__ void __launch_bounds__(256) bwd_finish_params(BwdParams p) {
 //   (the pairs of K with both indices >= k, and the w v terms of tokens >= k, cancel exactly
 //   and are left out rather than summed and subtracted: at fp32 that difference lost a
 //   decade of dA's digits), and ddt_k = A rc_k, dA += sum_k dt_k rc_k.
-// Kernels: the generic forward's first two give the state entering every chunk;
-// bwd_chunk_r forms C^T (e o dY) per chunk; bwd_state_reverse runs the adjoint backwards
-// over the chunks (each chunk's end adjoint left in place, and dinit); bwd_chunk_grad does
-// the rest, one CTA per chunk and head, every product in exact fp32 on the CUDA cores.
+// Kernels: bwd_chunk_sr forms each chunk's state B^T (w o X) and C^T (e o dY); the
+// generic forward's state passing turns the states into the state entering every chunk;
+// bwd_state_reverse runs the adjoint backwards over the chunks (each chunk's end adjoint
+// left in place, and dinit); bwd_chunk_grad does the rest, one CTA per chunk and head,
+// every product in exact fp32 on the CUDA cores.
 constexpr int kQc = 64;           // tokens per chunk
 constexpr int kCT = 256;          // threads of the chunk kernels
 
@@ -351,8 +352,8 @@ struct BwdCParams {
     const float *dt, *A, *D, *dfinal;
     void *dx;
     float *ddt, *dA, *dD, *dinit;
-    const float *states;   // (b, H, nc, N, P): the state entering each chunk
-    const float *csum;     // (b, H, nc): sum of dt A over each chunk
+    float *states;         // (b, H, nc, N, P): each chunk's state, then the state entering it
+    float *csum;           // (b, H, nc): sum of dt A over each chunk
     float *gst;            // (b, H, nc, N, P): C^T (e o dY), then the adjoint at each chunk's end
     float *dBh, *dCh;      // (b, T, H, N) per head
     int b, T, H, G, N, P, nc;
@@ -421,47 +422,66 @@ __device__ __forceinline__ void load_tile(float *dst, int ds, const IO *src, int
     }
 }
 
-// r = C^T (e o dY) of one chunk into gst.  Thread: column q of the state and R = N P / 256
-// consecutive state rows; the e o C rows are read as float4 broadcasts.
+// One chunk and head: its state s = B^T (w o X) into states and r = C^T (e o dY) into gst,
+// and the sum of dt A over it into csum.  Thread: column q of the state and R = N P / 256
+// consecutive state rows; the weighted B and C rows are read as float4 broadcasts.
 template <typename IO, int N, int P>
-__global__ void __launch_bounds__(kCT) bwd_chunk_r(BwdCParams p) {
+__global__ void __launch_bounds__(kCT) bwd_chunk_sr(BwdCParams p) {
     constexpr int Q = kQc, R = N * P / kCT;
     extern __shared__ float sm[];
-    float *sCe = sm;                  // [Q][N]
-    float *sdY = sCe + Q * N;         // [Q][P]
-    float *cum = sdY + Q * P;         // [Q]
-    float *ev = cum + Q;              // [Q]
+    float *sCe = sm;                  // [Q][N] e o C
+    float *sBw = sCe + Q * N;         // [Q][N] w o B
+    float *sdY = sBw + Q * N;         // [Q][P]
+    float *sX = sdY + Q * P;          // [Q][P]
+    float *cum = sX + Q * P;          // [Q]
+    float *ev = cum + Q, *wv = ev + Q;
     const int c = blockIdx.x, h = blockIdx.y, bi = blockIdx.z, tid = threadIdx.x;
     const int64_t t0 = (int64_t)c * Q;
     const int L = (int)min((int64_t)Q, (int64_t)p.T - t0);
     const int g = h / (p.H / p.G);
     const int64_t tok0 = (int64_t)bi * p.T + t0;
+    const int64_t bh = (int64_t)bi * p.H + h;
     load_tile<IO, Q, P>(sdY, P, static_cast<const IO *>(p.dy), tok0 * p.H * P + (int64_t)h * P, (int64_t)p.H * P, L);
+    load_tile<IO, Q, P>(sX, P, static_cast<const IO *>(p.x), tok0 * p.H * P + (int64_t)h * P, (int64_t)p.H * P, L);
     chunk_cum(p.dt + tok0 * p.H + h, p.H, p.A[h], L, cum);
-    if (tid < Q) ev[tid] = expf(cum[tid]);
+    if (tid < Q) {
+        ev[tid] = expf(cum[tid]);
+        wv[tid] = expf(cum[Q - 1] - cum[tid]);
+    }
+    if (tid == 0) p.csum[bh * p.nc + c] = cum[Q - 1];
     __syncthreads();
     load_tile<IO, Q, N>(sCe, N, static_cast<const IO *>(p.C), tok0 * p.G * N + (int64_t)g * N, (int64_t)p.G * N, L, ev);
+    load_tile<IO, Q, N>(sBw, N, static_cast<const IO *>(p.B), tok0 * p.G * N + (int64_t)g * N, (int64_t)p.G * N, L, wv);
     __syncthreads();
     const int q = tid % P, n0 = (tid / P) * R;
-    float acc[R];
+    float ar[R], as[R];
 #pragma unroll
-    for (int a = 0; a < R; ++a) acc[a] = 0.f;
+    for (int a = 0; a < R; ++a) ar[a] = as[a] = 0.f;
 #pragma unroll 2
     for (int k = 0; k < Q; ++k) {
-        const float d = sdY[k * P + q];
+        const float d = sdY[k * P + q], xv = sX[k * P + q];
         const float4 *ce = reinterpret_cast<const float4 *>(sCe + k * N + n0);
+        const float4 *bw = reinterpret_cast<const float4 *>(sBw + k * N + n0);
 #pragma unroll
         for (int a = 0; a < R / 4; ++a) {
-            const float4 v = ce[a];
-            acc[4 * a] = fmaf(v.x, d, acc[4 * a]);
-            acc[4 * a + 1] = fmaf(v.y, d, acc[4 * a + 1]);
-            acc[4 * a + 2] = fmaf(v.z, d, acc[4 * a + 2]);
-            acc[4 * a + 3] = fmaf(v.w, d, acc[4 * a + 3]);
+            const float4 v = ce[a], u = bw[a];
+            ar[4 * a] = fmaf(v.x, d, ar[4 * a]);
+            ar[4 * a + 1] = fmaf(v.y, d, ar[4 * a + 1]);
+            ar[4 * a + 2] = fmaf(v.z, d, ar[4 * a + 2]);
+            ar[4 * a + 3] = fmaf(v.w, d, ar[4 * a + 3]);
+            as[4 * a] = fmaf(u.x, xv, as[4 * a]);
+            as[4 * a + 1] = fmaf(u.y, xv, as[4 * a + 1]);
+            as[4 * a + 2] = fmaf(u.z, xv, as[4 * a + 2]);
+            as[4 * a + 3] = fmaf(u.w, xv, as[4 * a + 3]);
         }
     }
-    float *out = p.gst + (((int64_t)bi * p.H + h) * p.nc + c) * N * P;
+    float *outr = p.gst + (bh * p.nc + c) * N * P;
+    float *outs = p.states + (bh * p.nc + c) * N * P;
 #pragma unroll
-    for (int a = 0; a < R; ++a) out[(int64_t)(n0 + a) * P + q] = acc[a];
+    for (int a = 0; a < R; ++a) {
+        outr[(int64_t)(n0 + a) * P + q] = ar[a];
+        outs[(int64_t)(n0 + a) * P + q] = as[a];
+    }
 }
 
 // The adjoint chain over chunks, backwards, per (batch row, head, state entry): g starts at
@@ -832,14 +852,27 @@ BwdCLayout bwdc_layout(const Problem &p) {
 template <typename IO, int N>
 cudaError_t launch_chunked_typed(const Problem &p, const BwdCParams &cp, cudaStream_t s) {
     constexpr int P = 64;
-    const size_t sm_r = sizeof(float) * (size_t)(kQc * N + kQc * P + 2 * kQc);
+    const size_t sm_r = sizeof(float) * (size_t)(2 * kQc * N + 2 * kQc * P + 3 * kQc);
     const size_t sm_g = sizeof(float) * chunk_grad_floats<N, P>();
-    cudaError_t e = cudaFuncSetAttribute(bwd_chunk_r<IO, N, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_r);
+    cudaError_t e = cudaFuncSetAttribute(bwd_chunk_sr<IO, N, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_r);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(bwd_chunk_grad<IO, N, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_g);
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)cp.nc, (unsigned)p.H, (unsigned)p.b);
-    bwd_chunk_r<IO, N, P><<<grid, kCT, sm_r, s>>>(cp);
+    bwd_chunk_sr<IO, N, P><<<grid, kCT, sm_r, s>>>(cp);
+    // the state entering every chunk: the generic forward's state passing, in place
+    {
+        Problem q = p;
+        q.Q = kQc;
+        q.nc = cp.nc;
+        q.y = nullptr;
+        q.final_state = nullptr;
+        GenericWorkspace gw;
+        gw.status = nullptr;
+        gw.chunk_sum = cp.csum;
+        gw.states = cp.states;
+        if ((e = generic_passing_launch(q, gw, s)) != cudaSuccess) return e;
+    }
     bwd_state_reverse<<<dim3((unsigned)((N * P + kCT - 1) / kCT), (unsigned)p.H, (unsigned)p.b), kCT, 0, s>>>(cp);
     record_dominant_start(s);
     bwd_chunk_grad<IO, N, P><<<grid, kCT, sm_g, s>>>(cp);
@@ -850,24 +883,13 @@ cudaError_t launch_chunked_typed(const Problem &p, const BwdCParams &cp, cudaStr
 
 cudaError_t chunked_launch(const Problem &p, const BwdGrads &gr, char *base, cudaStream_t s) {
     const BwdCLayout l = bwdc_layout(p);
-    // the state entering every chunk: the generic forward's chunk-state and state-passing kernels
-    Problem q = p;
-    q.Q = kQc;
-    q.nc = l.nc;
-    q.y = nullptr;
-    q.final_state = nullptr;
-    GenericWorkspace gw;
-    gw.status = reinterpret_cast<int *>(base);
-    gw.chunk_sum = reinterpret_cast<float *>(base + l.off_cs);
-    gw.states = reinterpret_cast<float *>(base + l.off_st);
-    cudaError_t e = generic_states_launch(q, gw, s);
-    if (e != cudaSuccess) return e;
+    cudaError_t e;
     BwdCParams cp;
     cp.x = p.x; cp.B = p.B; cp.C = p.C; cp.dy = gr.dy;
     cp.dt = p.dt; cp.A = p.A; cp.D = p.D; cp.dfinal = gr.dfinal;
     cp.dx = gr.dx; cp.ddt = gr.ddt; cp.dA = gr.dA; cp.dD = gr.dD; cp.dinit = gr.dinit;
-    cp.states = gw.states;
-    cp.csum = gw.chunk_sum;
+    cp.states = reinterpret_cast<float *>(base + l.off_st);
+    cp.csum = reinterpret_cast<float *>(base + l.off_cs);
     cp.gst = reinterpret_cast<float *>(base + l.off_g);
     cp.dBh = reinterpret_cast<float *>(base + l.off_dbh);
     cp.dCh = reinterpret_cast<float *>(base + l.off_dch);

@@ -485,10 +485,11 @@ cudaError_t generic_launch(const Problem &p, const GenericWorkspace &w, cudaStre
     return launch_typed<float>(p, w, s);
 }
 
-cudaError_t generic_states_launch(const Problem &p, const GenericWorkspace &w, cudaStream_t s) {
-    cudaError_t e = p.io_dtype == SSD_DTYPE_BF16 ? launch_states<__nv_bfloat16>(p, w, s) : launch_states<float>(p, w, s);
-    if (e == cudaSuccess) note_launches(2);
-    return e;
+cudaError_t generic_passing_launch(const Problem &p, const GenericWorkspace &w, cudaStream_t s) {
+    dim3 g2((unsigned)((p.N * p.P + kThreads - 1) / kThreads), (unsigned)p.H, (unsigned)p.b);
+    gen_state_passing<<<g2, kThreads, 0, s>>>(p, w);
+    note_launches(1);
+    return cudaGetLastError();
 }
 
 }  // namespace ssd

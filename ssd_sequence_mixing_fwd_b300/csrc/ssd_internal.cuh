@@ -45,9 +45,9 @@ size_t generic_workspace_bytes(const Problem &p);
 GenericWorkspace generic_carve(const Problem &p, void *ws);
 bool generic_supports(const Problem &p);
 cudaError_t generic_launch(const Problem &p, const GenericWorkspace &w, cudaStream_t s);
-// chunk states and the state entering every chunk only (w.states, in place; p.final_state
-// written when set): the chunked backward's forward pass
-cudaError_t generic_states_launch(const Problem &p, const GenericWorkspace &w, cudaStream_t s);
+// the state passing alone: w.states holds every chunk's state s_c and w.chunk_sum its summed
+// log decay; leaves the state entering each chunk in place (p.final_state written when set)
+cudaError_t generic_passing_launch(const Problem &p, const GenericWorkspace &w, cudaStream_t s);
 
 // ---- fused tcgen05 path (csrc/ssd_fused_tc.cu) ----------------------------
 size_t fused_workspace_bytes(const Problem &p);
