@@ -195,3 +195,34 @@ def test_backward_argument_checks_enqueue_nothing(lib):
     d3 = dims(P=256, N=64)
     n = ctypes.c_size_t(0)
     assert lib.ssd_bwd_workspace_size(ctypes.byref(d3), ctypes.byref(n)) == ssd.SSD_ERR_UNSUPPORTED
+
+
+def a256(v):
+    return (v + 255) // 256 * 256
+
+
+@pytest.mark.parametrize("kw", [dict(b=2, T=100, H=4, P=64, N=128), dict(b=1, T=64, H=2, P=64, N=64),
+                                dict(b=3, T=1, H=6, P=64, N=128, G=3)])
+def test_backward_workspace_of_the_chunked_path(lib, kw):
+    # scalar A at P 64, N 64 / 128: states and adjoints (b H ceil(T/64) N P fp32 each), the chunk
+    # sums, per-head dB and dC (b T H N fp32 each), every region rounded up to 256 bytes
+    d = dims(path="auto", **kw)
+    b, T, H, P, N = kw["b"], kw["T"], kw["H"], kw["P"], kw["N"]
+    nc = -(-T // 64)
+    want = 256 + a256(4 * b * H * nc) + a256(4 * b * H * nc * N * P) * 2 + a256(4 * b * T * H * N) * 2
+    assert ssd.ssd_bwd_workspace_size(d) == want
+
+
+def test_backward_workspace_of_the_recurrence_path(lib):
+    # diagonal A (and other head dims): checkpoints b H ceil(N / (1024 / P)) ceil(T / 8) x 4 KB and
+    # three b T H N fp32 arrays plus the b T H P dx accumulator
+    for kw in (dict(b=2, T=100, H=4, P=64, N=64, a_mode="diagonal"), dict(b=1, T=33, H=2, P=32, N=16)):
+        d = dims(path="auto", **kw)
+        b, T, H, P, N = kw["b"], kw["T"], kw["H"], kw["P"], kw["N"]
+        nsl = -(-N // (1024 // P))
+        want = 256 + a256(4 * b * H * nsl * -(-T // 8) * 1024)
+        want = a256(want + 4 * b * T * H * N)
+        want = a256(want + 4 * b * T * H * N)
+        want = a256(want + 4 * b * T * H * N)
+        want = a256(want + 4 * b * T * H * P)
+        assert ssd.ssd_bwd_workspace_size(d) == want
