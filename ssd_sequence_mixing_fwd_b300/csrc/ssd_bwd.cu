@@ -424,9 +424,10 @@ __device__ __forceinline__ void load_tile(float *dst, int ds, const IO *src, int
 
 // One chunk and head: its state s = B^T (w o X) into states and r = C^T (e o dY) into gst,
 // and the sum of dt A over it into csum.  Thread: column q of the state and R = N P / 256
-// consecutive state rows; the weighted B and C rows are read as float4 broadcasts.
+// consecutive state rows; the weighted B and C rows are read as float4 broadcasts.  Two CTAs
+// per SM (99 KB of shared memory each at N 128; registers capped at 128 for it).
 template <typename IO, int N, int P>
-__global__ void __launch_bounds__(kCT) bwd_chunk_sr(BwdCParams p) {
+__global__ void __launch_bounds__(kCT, 2) bwd_chunk_sr(BwdCParams p) {
     constexpr int Q = kQc, R = N * P / kCT;
     extern __shared__ float sm[];
     float *sCe = sm;                  // [Q][N] e o C
