@@ -229,6 +229,9 @@ SSD_API int ssd_decode_step(const ssd_dims *dims,
  *   dB, dC (b,T,G,N) io dtype (summed over the heads of each group)
  *   dD (H) float32 or NULL (not computed; sum of dy . x per head)
  *   dinit (b,H,N,P) float32 or NULL (not computed)
+ * dA and dD are sums over chunks (or token ranges) added with fp32 atomics,
+ * so they may differ in the last bits from one call to the next; every other
+ * output is reproducible.
  * dims->path must be SSD_PATH_AUTO or SSD_PATH_GENERIC (SSD_ERR_UNSUPPORTED
  * otherwise); the backward takes 4 <= P <= 128.  Every pointer 16-byte
  * aligned; workspace >= ssd_bwd_workspace_size bytes, 256-byte aligned
