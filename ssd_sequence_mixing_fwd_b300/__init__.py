@@ -244,6 +244,12 @@ def ssd_fwd(x, dt, A, B, C, D=None, init_state=None, chunk_Q=256, return_final_s
     return y, final_state
 
 
+def fwd(x, dt, A, B, C, D=None, init_state=None, chunk=256, return_final_state=True, **kw):
+    """``ssd_fwd`` under its short name: ``(y, final_state)`` for chunk length ``chunk``
+    (``final_state`` is None unless ``return_final_state``).  Raises :class:`SSDError`."""
+    return ssd_fwd(x, dt, A, B, C, D, init_state, chunk_Q=chunk, return_final_state=return_final_state, **kw)
+
+
 def ssd_scan(x, dt, A, B, C, D=None, init_state=None, return_final_state=True, y=None, final_state=None,
              stream=None):
     """The same map as :func:`ssd_fwd`, evaluated by the linear recurrence token by token on CUDA

@@ -214,3 +214,15 @@ def test_split_sequence_composition_gpu(cuda_device):
     yr, fr = oracle.recurrence(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"], inp["init_state"])
     assert rel(np.concatenate([y1, y2], axis=1), yr) <= 2e-3
     assert rel(f2, fr) <= 2e-3
+
+
+def test_short_name_fwd_matches_ssd_fwd(cuda_device):
+    # ssd.fwd is ssd_fwd under its short name: the same kernels, bit for bit
+    w = Workload("t", b=1, T=300, H=4, P=64, N=128, G=2, Q=128, D="normal", init_std=0.1, seed=931)
+    d = {k: (None if v is None else v.to(cuda_device)) for k, v in make_inputs(w).items()}
+    y1, f1 = ssd.fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["init_state"], chunk=w.Q)
+    y2, f2 = ssd.ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["init_state"], chunk_Q=w.Q)
+    y3, f3 = ssd.fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["init_state"], chunk=w.Q,
+                     return_final_state=False)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2) and torch.equal(f1, f2) and torch.equal(y1, y3) and f3 is None
