@@ -236,7 +236,8 @@ SSD_API int ssd_decode_step(const ssd_dims *dims,
  * otherwise); the backward takes 4 <= P <= 128.  Every pointer 16-byte
  * aligned; workspace >= ssd_bwd_workspace_size bytes, 256-byte aligned
  * (chunked path: two fp32 arrays of b*H*ceil(T/64)*N*P floats -- the states
- * and the adjoints -- plus 2*b*T*H*N floats of per-head dB and dC; the
+ * and the adjoints -- plus 2*b*T*H*N floats of per-head dB and dC and
+ * b*ceil(T/64)*G*64*64 floats of C B^T per chunk and group; the
  * other path: checkpoints b*H*ceil(N/(1024/P))*ceil(T/8)*4 KB plus fp32
  * per-token arrays of 3*b*T*H*N + b*T*H*P floats; each region rounded up to
  * 256 bytes).  Asynchronous on `stream`; on any

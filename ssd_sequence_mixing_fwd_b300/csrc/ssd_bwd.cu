@@ -339,7 +339,8 @@ __global__ void __launch_bounds__(256) bwd_finish_params(BwdParams p) {
 //   (the pairs of K with both indices >= k, and the w v terms of tokens >= k, cancel exactly
 //   and are left out rather than summed and subtracted: at fp32 that difference lost a
 //   decade of dA's digits), and ddt_k = A rc_k, dA += sum_k dt_k rc_k.
-// Kernels: bwd_chunk_sr forms each chunk's state B^T (w o X) and C^T (e o dY); the
+// Kernels: bwd_chunk_cb forms C B^T once per chunk and B/C group (all the group's heads
+// share it); bwd_chunk_sr forms each chunk's state B^T (w o X) and C^T (e o dY); the
 // generic forward's state passing turns the states into the state entering every chunk;
 // bwd_state_reverse runs the adjoint backwards over the chunks (each chunk's end adjoint
 // left in place, and dinit); bwd_chunk_grad does the rest, one CTA per chunk and head,
@@ -356,6 +357,7 @@ struct BwdCParams {
     float *csum;           // (b, H, nc): sum of dt A over each chunk
     float *gst;            // (b, H, nc, N, P): C^T (e o dY), then the adjoint at each chunk's end
     float *dBh, *dCh;      // (b, T, H, N) per head
+    float *cbg;            // (b, nc, G, Q, Q): C B^T of each chunk and B/C group
     int b, T, H, G, N, P, nc;
 };
 
@@ -420,6 +422,35 @@ __device__ __forceinline__ void load_tile(float *dst, int ds, const IO *src, int
             for (int v = 0; v < V; ++v) dst[k * ds + c + v] = sc * f[v];
         }
     }
+}
+
+// C B^T of one chunk and B/C group into cbg: Q x Q (both triangles; the heads take j <= i),
+// one CTA, 4 x 4 tiles, the products' odd-stride shared-memory layout.
+template <int RM, int CN> __device__ __forceinline__ void zero(float (&acc)[RM][CN]);
+template <int RM, int CN>
+__device__ __forceinline__ void mm(float (&acc)[RM][CN], const float *A, int am, int ak, const float *Bm, int bk,
+                                   int bn, int K, int tm, int tn);
+template <typename IO, int N>
+__global__ void __launch_bounds__(kCT) bwd_chunk_cb(BwdCParams p) {
+    constexpr int Q = kQc, NS = N + 1, RM = Q / 16, CQ = Q / 16;
+    extern __shared__ float sm[];
+    float *sB = sm, *sC = sm + Q * NS;
+    const int c = blockIdx.x, g = blockIdx.y, bi = blockIdx.z, tid = threadIdx.x;
+    const int64_t t0 = (int64_t)c * Q;
+    const int L = (int)min((int64_t)Q, (int64_t)p.T - t0);
+    const int64_t tok0 = (int64_t)bi * p.T + t0;
+    load_tile<IO, Q, N>(sB, NS, static_cast<const IO *>(p.B), tok0 * p.G * N + (int64_t)g * N, (int64_t)p.G * N, L);
+    load_tile<IO, Q, N>(sC, NS, static_cast<const IO *>(p.C), tok0 * p.G * N + (int64_t)g * N, (int64_t)p.G * N, L);
+    __syncthreads();
+    const int tm = tid >> 4, tn = tid & 15;
+    float acb[RM][CQ];
+    zero(acb);
+    mm(acb, sC, NS, 1, sB, 1, NS, N, tm, tn);
+    float *out = p.cbg + (((int64_t)bi * p.nc + c) * p.G + g) * Q * Q;
+#pragma unroll
+    for (int a = 0; a < RM; ++a)
+#pragma unroll
+        for (int j = 0; j < CQ; ++j) out[(tm + 16 * a) * Q + tn + 16 * j] = acb[a][j];
 }
 
 // One chunk and head: its state s = B^T (w o X) into states and r = C^T (e o dY) into gst,
@@ -606,12 +637,17 @@ __global__ void __launch_bounds__(kCT, 1) bwd_chunk_grad(BwdCParams p) {
     }
     __syncthreads();
 
-    // C B^T and dY X^T; S, G and K = G o (C B^T)
+    // C B^T (formed once per group) and dY X^T; S, G and K = G o (C B^T)
     {
         float acb[RM][CQ], ayx[RM][CQ];
-        zero(acb);
+        {
+            const float *cb = p.cbg + (((int64_t)bi * p.nc + c) * p.G + g) * Q * Q;
+#pragma unroll
+            for (int a = 0; a < RM; ++a)
+#pragma unroll
+                for (int j = 0; j < CQ; ++j) acb[a][j] = __ldg(cb + (tm + 16 * a) * Q + tn + 16 * j);
+        }
         zero(ayx);
-        mm(acb, sC, NS, 1, sB, 1, NS, N, tm, tn);
         mm(ayx, sdY, PS, 1, sX, 1, PS, P, tm, tn);
 #pragma unroll
         for (int a = 0; a < RM; ++a) {
@@ -834,7 +870,7 @@ bool chunked_applies(const Problem &p) {
 
 struct BwdCLayout {
     int64_t nc;
-    size_t off_cs, off_st, off_g, off_dbh, off_dch, total;
+    size_t off_cs, off_st, off_g, off_dbh, off_dch, off_cb, total;
 };
 
 BwdCLayout bwdc_layout(const Problem &p) {
@@ -846,7 +882,8 @@ BwdCLayout bwdc_layout(const Problem &p) {
     l.off_g = align_up(l.off_st + sizeof(float) * np, 256);
     l.off_dbh = align_up(l.off_g + sizeof(float) * np, 256);
     l.off_dch = align_up(l.off_dbh + sizeof(float) * tokh * p.N, 256);
-    l.total = align_up(l.off_dch + sizeof(float) * tokh * p.N, 256);
+    l.off_cb = align_up(l.off_dch + sizeof(float) * tokh * p.N, 256);
+    l.total = align_up(l.off_cb + sizeof(float) * (size_t)(p.b * l.nc * p.G) * kQc * kQc, 256);
     return l;
 }
 
@@ -859,6 +896,11 @@ cudaError_t launch_chunked_typed(const Problem &p, const BwdCParams &cp, cudaStr
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(bwd_chunk_grad<IO, N, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_g);
     if (e != cudaSuccess) return e;
+    const size_t sm_cb = sizeof(float) * (size_t)(2 * kQc * (N + 1));
+    if ((e = cudaFuncSetAttribute(bwd_chunk_cb<IO, N>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_cb)) !=
+        cudaSuccess)
+        return e;
+    bwd_chunk_cb<IO, N><<<dim3((unsigned)cp.nc, (unsigned)p.G, (unsigned)p.b), kCT, sm_cb, s>>>(cp);
     const dim3 grid((unsigned)cp.nc, (unsigned)p.H, (unsigned)p.b);
     bwd_chunk_sr<IO, N, P><<<grid, kCT, sm_r, s>>>(cp);
     // the state entering every chunk: the generic forward's state passing, in place
@@ -878,7 +920,7 @@ cudaError_t launch_chunked_typed(const Problem &p, const BwdCParams &cp, cudaStr
     record_dominant_start(s);
     bwd_chunk_grad<IO, N, P><<<grid, kCT, sm_g, s>>>(cp);
     record_dominant_stop(s);
-    note_launches(3);
+    note_launches(4);
     return cudaGetLastError();
 }
 
@@ -894,6 +936,7 @@ cudaError_t chunked_launch(const Problem &p, const BwdGrads &gr, char *base, cud
     cp.gst = reinterpret_cast<float *>(base + l.off_g);
     cp.dBh = reinterpret_cast<float *>(base + l.off_dbh);
     cp.dCh = reinterpret_cast<float *>(base + l.off_dch);
+    cp.cbg = reinterpret_cast<float *>(base + l.off_cb);
     cp.b = (int)p.b; cp.T = (int)p.T; cp.H = (int)p.H; cp.G = (int)p.G; cp.N = (int)p.N; cp.P = (int)p.P;
     cp.nc = (int)l.nc;
     const bool bf = p.io_dtype == SSD_DTYPE_BF16;

@@ -132,12 +132,13 @@ def bwd_chunked_applies(w: Workload) -> bool:
 
 def algorithmic_flops_bwd(w: Workload, Q: int = 64) -> float:
     """Causal work of the chunked backward on Q-token chunks (every product a multiply-add
-    pair): per chunk and head, C B^T, dY X^T, S^T dY, G B and G^T C on the causal triangle
-    (1.5 Q^2 N + Q^2 P) and the five rank-N products B g, dY h^T, X g^T, C^T (e o dY) and
-    the chunk state B^T (w o X) (5 Q N P)."""
+    pair): per chunk and head, dY X^T, S^T dY, G B and G^T C on the causal triangle
+    (Q^2 N + Q^2 P) and the five rank-N products B g, dY h^T, X g^T, C^T (e o dY) and the
+    chunk state B^T (w o X) (5 Q N P); per chunk and B/C group, C B^T (Q^2 N / 2)."""
     nc = -(-w.T // Q)
-    per = 1.5 * Q * Q * w.N + Q * Q * w.P + 5 * Q * w.N * w.P
-    return 2.0 * per * w.b * w.H * nc
+    per_head = Q * Q * w.N + Q * Q * w.P + 5 * Q * w.N * w.P
+    per_group = 0.5 * Q * Q * w.N
+    return 2.0 * nc * w.b * (per_head * w.H + per_group * w.G)
 
 
 def algorithmic_flops(w: Workload) -> float:
