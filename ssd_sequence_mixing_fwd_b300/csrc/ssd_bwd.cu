@@ -454,12 +454,12 @@ __global__ void __launch_bounds__(kCT) bwd_chunk_cb(BwdCParams p) {
 }
 
 // One chunk and head: its state s = B^T (w o X) into states and r = C^T (e o dY) into gst,
-// and the sum of dt A over it into csum.  Thread: column q of the state and R = N P / 256
-// consecutive state rows; the weighted B and C rows are read as float4 broadcasts.  Two CTAs
-// per SM (99 KB of shared memory each at N 128; registers capped at 128 for it).
+// and the sum of dt A over it into csum.  Both N x P products in the 2-D tiles of mm (thread
+// (tm, tn): state rows tm + 16 a, columns tn + 16 j), whose loads are one wavefront each.  Two
+// CTAs per SM (99 KB of shared memory each at N 128; registers capped at 128 for it).
 template <typename IO, int N, int P>
 __global__ void __launch_bounds__(kCT, 2) bwd_chunk_sr(BwdCParams p) {
-    constexpr int Q = kQc, R = N * P / kCT;
+    constexpr int Q = kQc;
     extern __shared__ float sm[];
     float *sCe = sm;                  // [Q][N] e o C
     float *sBw = sCe + Q * N;         // [Q][N] w o B
@@ -485,35 +485,23 @@ __global__ void __launch_bounds__(kCT, 2) bwd_chunk_sr(BwdCParams p) {
     load_tile<IO, Q, N>(sCe, N, static_cast<const IO *>(p.C), tok0 * p.G * N + (int64_t)g * N, (int64_t)p.G * N, L, ev);
     load_tile<IO, Q, N>(sBw, N, static_cast<const IO *>(p.B), tok0 * p.G * N + (int64_t)g * N, (int64_t)p.G * N, L, wv);
     __syncthreads();
-    const int q = tid % P, n0 = (tid / P) * R;
-    float ar[R], as[R];
-#pragma unroll
-    for (int a = 0; a < R; ++a) ar[a] = as[a] = 0.f;
-#pragma unroll 2
-    for (int k = 0; k < Q; ++k) {
-        const float d = sdY[k * P + q], xv = sX[k * P + q];
-        const float4 *ce = reinterpret_cast<const float4 *>(sCe + k * N + n0);
-        const float4 *bw = reinterpret_cast<const float4 *>(sBw + k * N + n0);
-#pragma unroll
-        for (int a = 0; a < R / 4; ++a) {
-            const float4 v = ce[a], u = bw[a];
-            ar[4 * a] = fmaf(v.x, d, ar[4 * a]);
-            ar[4 * a + 1] = fmaf(v.y, d, ar[4 * a + 1]);
-            ar[4 * a + 2] = fmaf(v.z, d, ar[4 * a + 2]);
-            ar[4 * a + 3] = fmaf(v.w, d, ar[4 * a + 3]);
-            as[4 * a] = fmaf(u.x, xv, as[4 * a]);
-            as[4 * a + 1] = fmaf(u.y, xv, as[4 * a + 1]);
-            as[4 * a + 2] = fmaf(u.z, xv, as[4 * a + 2]);
-            as[4 * a + 3] = fmaf(u.w, xv, as[4 * a + 3]);
-        }
-    }
+    constexpr int RN = N / 16, CP = P / 16;
+    const int tm = tid >> 4, tn = tid & 15;
+    float ar[RN][CP], as[RN][CP];
+    zero(ar);
+    zero(as);
+    mm(ar, sCe, 1, N, sdY, P, 1, Q, tm, tn);      // A(n, k) = (e o C)[k][n], Bop(k, q) = dY[k][q]
+    mm(as, sBw, 1, N, sX, P, 1, Q, tm, tn);       // A(n, k) = (w o B)[k][n], Bop(k, q) = X[k][q]
     float *outr = p.gst + (bh * p.nc + c) * N * P;
     float *outs = p.states + (bh * p.nc + c) * N * P;
 #pragma unroll
-    for (int a = 0; a < R; ++a) {
-        outr[(int64_t)(n0 + a) * P + q] = ar[a];
-        outs[(int64_t)(n0 + a) * P + q] = as[a];
-    }
+    for (int a = 0; a < RN; ++a)
+#pragma unroll
+        for (int j = 0; j < CP; ++j) {
+            const int64_t o = (int64_t)(tm + 16 * a) * P + tn + 16 * j;
+            outr[o] = ar[a][j];
+            outs[o] = as[a][j];
+        }
 }
 
 // The adjoint chain over chunks, backwards, per (batch row, head, state entry): g starts at
