@@ -121,3 +121,41 @@ def test_backward_empty_and_rejections(cuda_device):
         with pytest.raises(ssd.SSDError) as e:
             ssd.ssd_bwd_workspace_size(d)
         assert e.value.status == ssd.SSD_ERR_UNSUPPORTED
+
+
+def test_backward_at_the_2p7b_bench_shape(cuda_device):
+    """The bench's backward call at the full 2.7B shape (b4 T8192 H80 P64 N128 G1), checked on two
+    whole heads: every batch row's dx, ddt and dinit of the head, and the head's dA and dD (sums
+    over all batch rows and tokens), against the fp64 backward oracle run on that head alone (with
+    one B/C group, a head's gradients depend on its own inputs and the shared B and C only).
+
+    dA = sum_k dt_k rc_k and dD = sum dy x are sums of 32768 (and 2M) terms of both signs; for head
+    0 here |dA| = 0.53 while sum_k |dt_k rc_k| = 8.7e3.  A sum of terms that each carry a few fp32
+    rounding errors is only held to about eps_32 * sum |terms| (the forward error bound of
+    summation), so these two scalars get 1e-4 relative plus 2 eps_32 sum |terms|, the terms taken
+    from the oracle (dt ddt / A for dA, dy x for dD)."""
+    from ssd_sequence_mixing_fwd_b300.inputs import WORKLOADS
+    w = WORKLOADS["mamba2_2p7b"]
+    inp = make_inputs(w)
+    dy, df = cotangents(w, 4242, True)
+    d = {k: (None if v is None else v.to(cuda_device)) for k, v in inp.items()}
+    got = ssd.ssd_bwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["init_state"], dy.to(cuda_device),
+                      df.to(cuda_device))
+    torch.cuda.synchronize()
+    got = {k: (None if v is None else v.float().cpu().numpy()) for k, v in got.items()}
+    for h in (0, 57):
+        sl = lambda t: None if t is None else t[:, :, h:h + 1].contiguous()
+        ref = oracle.recurrence_bwd(sl(inp["x"]), sl(inp["dt"]), inp["A"][h:h + 1], inp["B"], inp["C"],
+                                    None if inp["D"] is None else inp["D"][h:h + 1],
+                                    None if inp["init_state"] is None else inp["init_state"][:, h:h + 1],
+                                    dy[:, :, h:h + 1].double().numpy(), df[:, h:h + 1].double().numpy())
+        assert rel(got["dx"][:, :, h], ref["dx"][:, :, 0]) <= 2e-3
+        assert rel(got["ddt"][:, :, h], ref["ddt"][:, :, 0]) <= 1e-4
+        assert rel(got["dinit"][:, h], ref["dinit"][:, 0]) <= 1e-4
+        eps = 2.0 ** -24
+        dt_h = inp["dt"][:, :, h].double().numpy()
+        terms_a = np.abs(dt_h * ref["ddt"][:, :, 0] / float(inp["A"][h])).sum()
+        assert abs(got["dA"][h] - ref["dA"][0]) <= 1e-4 * abs(ref["dA"][0]) + 2 * eps * terms_a
+        if ref["dD"] is not None:
+            terms_d = np.abs(dy[:, :, h].double().numpy() * inp["x"][:, :, h].double().numpy()).sum()
+            assert abs(got["dD"][h] - ref["dD"][0]) <= 1e-4 * abs(ref["dD"][0]) + 2 * eps * terms_d
