@@ -561,6 +561,53 @@ __device__ __forceinline__ void mm(float (&acc)[RM][CN], const float *A, int am,
     }
 }
 
+// The same product where the contraction runs over a triangle of a Q x Q factor (Q = 16 RM):
+// output row m_a = tm + 16 a takes k in the 16-wide blocks s <= a (LOWER: A(m, k) = 0 for
+// k > m's block) or s >= a (upper).  Row a's block is a for every thread, so every thread
+// skips the same segments; inside the row's own block the zeros of the triangle are
+// multiplied as they are.
+template <int RM, int CN, bool LOWER>
+__device__ __forceinline__ void mm_tri(float (&acc)[RM][CN], const float *A, int am, int ak, const float *Bm, int bk,
+                                       int bn, int tm, int tn) {
+#pragma unroll
+    for (int sg = 0; sg < RM; ++sg) {
+#pragma unroll 8
+        for (int k = 16 * sg; k < 16 * sg + 16; ++k) {
+            float av[RM], bv[CN];
+#pragma unroll
+            for (int a = 0; a < RM; ++a)
+                if (LOWER ? a >= sg : a <= sg) av[a] = A[(tm + 16 * a) * am + k * ak];
+#pragma unroll
+            for (int j = 0; j < CN; ++j) bv[j] = Bm[k * bk + (tn + 16 * j) * bn];
+#pragma unroll
+            for (int a = 0; a < RM; ++a)
+                if (LOWER ? a >= sg : a <= sg) {
+#pragma unroll
+                    for (int j = 0; j < CN; ++j) acc[a][j] = fmaf(av[a], bv[j], acc[a][j]);
+                }
+        }
+    }
+}
+
+// The product on the lower block triangle of a Q x Q output (column blocks j <= row block a).
+template <int RM, int CN>
+__device__ __forceinline__ void mm_lowout(float (&acc)[RM][CN], const float *A, int am, int ak, const float *Bm,
+                                          int bk, int bn, int K, int tm, int tn) {
+#pragma unroll 8
+    for (int k = 0; k < K; ++k) {
+        float av[RM], bv[CN];
+#pragma unroll
+        for (int a = 0; a < RM; ++a) av[a] = A[(tm + 16 * a) * am + k * ak];
+#pragma unroll
+        for (int j = 0; j < CN; ++j) bv[j] = Bm[k * bk + (tn + 16 * j) * bn];
+#pragma unroll
+        for (int a = 0; a < RM; ++a)
+#pragma unroll
+            for (int j = 0; j < CN; ++j)
+                if (j <= a) acc[a][j] = fmaf(av[a], bv[j], acc[a][j]);
+    }
+}
+
 template <int RM, int CN> __device__ __forceinline__ void zero(float (&acc)[RM][CN]) {
 #pragma unroll
     for (int a = 0; a < RM; ++a)
@@ -636,7 +683,7 @@ __global__ void __launch_bounds__(kCT, 1) bwd_chunk_grad(BwdCParams p) {
                 for (int j = 0; j < CQ; ++j) acb[a][j] = __ldg(cb + (tm + 16 * a) * Q + tn + 16 * j);
         }
         zero(ayx);
-        mm(ayx, sdY, PS, 1, sX, 1, PS, P, tm, tn);
+        mm_lowout(ayx, sdY, PS, 1, sX, 1, PS, P, tm, tn);        // only j <= i is used
 #pragma unroll
         for (int a = 0; a < RM; ++a) {
             const int i = tm + 16 * a;
@@ -662,7 +709,7 @@ __global__ void __launch_bounds__(kCT, 1) bwd_chunk_grad(BwdCParams p) {
         float asd[RM][CP], abg[RM][CP];
         zero(asd);
         zero(abg);
-        mm(asd, sS, 1, QS, sdY, PS, 1, Q, tm, tn);
+        mm_tri<RM, CP, false>(asd, sS, 1, QS, sdY, PS, 1, tm, tn);   // sum over i >= j
         mm(abg, sB, NS, 1, sGc, PS, 1, N, tm, tn);
         const float Dh = p.D ? p.D[h] : 0.f;
         IO *dx = static_cast<IO *>(p.dx);
@@ -692,7 +739,7 @@ __global__ void __launch_bounds__(kCT, 1) bwd_chunk_grad(BwdCParams p) {
         float agb[RM][CN], ayh[RM][CN];
         zero(agb);
         zero(ayh);
-        mm(agb, sG, QS, 1, sB, NS, 1, Q, tm, tn);
+        mm_tri<RM, CN, true>(agb, sG, QS, 1, sB, NS, 1, tm, tn);    // sum over j <= i
         mm(ayh, sdY, PS, 1, sH, 1, PS, P, tm, tn);
 #pragma unroll
         for (int a = 0; a < RM; ++a) {
@@ -714,7 +761,7 @@ __global__ void __launch_bounds__(kCT, 1) bwd_chunk_grad(BwdCParams p) {
         float agc[RM][CN], axg[RM][CN];
         zero(agc);
         zero(axg);
-        mm(agc, sG, 1, QS, sC, NS, 1, Q, tm, tn);
+        mm_tri<RM, CN, false>(agc, sG, 1, QS, sC, NS, 1, tm, tn);   // sum over i >= j
         mm(axg, sX, PS, 1, sGc, 1, PS, P, tm, tn);
 #pragma unroll
         for (int a = 0; a < RM; ++a) {
