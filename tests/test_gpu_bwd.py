@@ -83,6 +83,9 @@ CASES = [
                                      seed=723)),
     ("chunked_bf16_N128_G2_T200", Workload("t", b=2, T=200, H=6, P=64, N=128, G=2, Q=256, D="none",
                                            init_std=0.1, seed=724)),
+    # the long-sequence head dims (N 256, one head per B/C group): the recurrence path, 16 slices
+    ("scalar_bf16_N256_G8", Workload("t", b=1, T=150, H=8, P=64, N=256, G=8, Q=128, D="none", init_std=0.1,
+                                     seed=725)),
 ]
 
 
