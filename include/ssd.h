@@ -211,8 +211,9 @@ SSD_API int ssd_decode_step(const ssd_dims *dims,
  * weighs; the pages give no backward, so this is the chain rule of the
  * recurrence of "The recurrence as one matrix").  CUDA cores, fp32
  * arithmetic, two paths:
- *  - scalar A with P == 64 and N in {64, 128}: the chunked algorithm run
- *    backwards on 64-token chunks -- the state entering every chunk (the
+ *  - scalar A with P == 64 and N in {64, 128, 256}: the chunked algorithm
+ *    run backwards on Q-token chunks (Q = 64; 32 at N = 256) -- the state
+ *    entering every chunk (the
  *    generic forward's chunk-state kernels), the adjoint at every chunk's
  *    end (a reverse scan over chunks), then per chunk and head the dense
  *    products of the quadratic form and the rank-N terms;
@@ -235,9 +236,9 @@ SSD_API int ssd_decode_step(const ssd_dims *dims,
  * dims->path must be SSD_PATH_AUTO or SSD_PATH_GENERIC (SSD_ERR_UNSUPPORTED
  * otherwise); the backward takes 4 <= P <= 128.  Every pointer 16-byte
  * aligned; workspace >= ssd_bwd_workspace_size bytes, 256-byte aligned
- * (chunked path: two fp32 arrays of b*H*ceil(T/64)*N*P floats -- the states
- * and the adjoints -- plus 2*b*T*H*N floats of per-head dB and dC and
- * b*ceil(T/64)*G*64*64 floats of C B^T per chunk and group; the
+ * (chunked path, Q as above: two fp32 arrays of b*H*ceil(T/Q)*N*P floats --
+ * the states and the adjoints -- plus 2*b*T*H*N floats of per-head dB and dC
+ * and b*ceil(T/Q)*G*Q*Q floats of C B^T per chunk and group; the
  * other path: checkpoints b*H*ceil(N/(1024/P))*ceil(T/8)*4 KB plus fp32
  * per-token arrays of 3*b*T*H*N + b*T*H*P floats; each region rounded up to
  * 256 bytes).  Asynchronous on `stream`; on any

@@ -345,7 +345,8 @@ __global__ void __launch_bounds__(256) bwd_finish_params(BwdParams p) {
 // bwd_state_reverse runs the adjoint backwards over the chunks (each chunk's end adjoint
 // left in place, and dinit); bwd_chunk_grad does the rest, one CTA per chunk and head,
 // every product in exact fp32 on the CUDA cores.
-constexpr int kQc = 64;           // tokens per chunk
+// tokens per chunk: 64, or 32 at N = 256 (the product kernel's shared memory then still fits)
+template <int N> constexpr int chunk_len() { return N > 128 ? 32 : 64; }
 constexpr int kCT = 256;          // threads of the chunk kernels
 
 struct BwdCParams {
@@ -363,8 +364,9 @@ struct BwdCParams {
 
 // cum[0..Q): inclusive prefix sum of dt A over the chunk (dt of token k at dt[k * stride];
 // zero past L, so the sum holds its last value there).  All threads of the block.
+template <int Q>
 __device__ __forceinline__ void chunk_cum(const float *dt, int64_t stride, float Ah, int L, float *cum) {
-    if (threadIdx.x < kQc) {
+    if (threadIdx.x < Q) {
         const int i = threadIdx.x;
         float v = i < L ? dt[i * stride] * Ah : 0.f;
 #pragma unroll
@@ -375,7 +377,7 @@ __device__ __forceinline__ void chunk_cum(const float *dt, int64_t stride, float
         cum[i] = v;
     }
     __syncthreads();
-    if (threadIdx.x >= 32 && threadIdx.x < kQc) cum[threadIdx.x] += cum[31];
+    if (threadIdx.x >= 32 && threadIdx.x < Q) cum[threadIdx.x] += cum[31];
     __syncthreads();
 }
 
@@ -432,7 +434,7 @@ __device__ __forceinline__ void mm(float (&acc)[RM][CN], const float *A, int am,
                                    int bn, int K, int tm, int tn);
 template <typename IO, int N>
 __global__ void __launch_bounds__(kCT) bwd_chunk_cb(BwdCParams p) {
-    constexpr int Q = kQc, NS = N + 1, RM = Q / 16, CQ = Q / 16;
+    constexpr int Q = chunk_len<N>(), NS = N + 1, RM = Q / 16, CQ = Q / 16;
     extern __shared__ float sm[];
     float *sB = sm, *sC = sm + Q * NS;
     const int c = blockIdx.x, g = blockIdx.y, bi = blockIdx.z, tid = threadIdx.x;
@@ -458,8 +460,8 @@ __global__ void __launch_bounds__(kCT) bwd_chunk_cb(BwdCParams p) {
 // (tm, tn): state rows tm + 16 a, columns tn + 16 j), whose loads are one wavefront each.  Two
 // CTAs per SM (99 KB of shared memory each at N 128; registers capped at 128 for it).
 template <typename IO, int N, int P>
-__global__ void __launch_bounds__(kCT, 2) bwd_chunk_sr(BwdCParams p) {
-    constexpr int Q = kQc;
+__global__ void __launch_bounds__(kCT, N > 128 ? 1 : 2) bwd_chunk_sr(BwdCParams p) {
+    constexpr int Q = chunk_len<N>();
     extern __shared__ float sm[];
     float *sCe = sm;                  // [Q][N] e o C
     float *sBw = sCe + Q * N;         // [Q][N] w o B
@@ -475,7 +477,7 @@ __global__ void __launch_bounds__(kCT, 2) bwd_chunk_sr(BwdCParams p) {
     const int64_t bh = (int64_t)bi * p.H + h;
     load_tile<IO, Q, P>(sdY, P, static_cast<const IO *>(p.dy), tok0 * p.H * P + (int64_t)h * P, (int64_t)p.H * P, L);
     load_tile<IO, Q, P>(sX, P, static_cast<const IO *>(p.x), tok0 * p.H * P + (int64_t)h * P, (int64_t)p.H * P, L);
-    chunk_cum(p.dt + tok0 * p.H + h, p.H, p.A[h], L, cum);
+    chunk_cum<Q>(p.dt + tok0 * p.H + h, p.H, p.A[h], L, cum);
     if (tid < Q) {
         ev[tid] = expf(cum[tid]);
         wv[tid] = expf(cum[Q - 1] - cum[tid]);
@@ -624,12 +626,13 @@ __device__ __forceinline__ float sum16(float v) {
 
 template <int N, int P>
 constexpr size_t chunk_grad_floats() {
-    return 8 + (size_t)2 * kQc * (P + 1) + 2 * kQc * (N + 1) + 2 * N * (P + 1) + 3 * kQc * (kQc + 1) + 5 * kQc;
+    constexpr int Q = chunk_len<N>();
+    return 8 + (size_t)2 * Q * (P + 1) + 2 * Q * (N + 1) + 2 * N * (P + 1) + 3 * Q * (Q + 1) + 5 * Q;
 }
 
 template <typename IO, int N, int P>
 __global__ void __launch_bounds__(kCT, 1) bwd_chunk_grad(BwdCParams p) {
-    constexpr int Q = kQc, QS = Q + 1, PS = P + 1, NS = N + 1;
+    constexpr int Q = chunk_len<N>(), QS = Q + 1, PS = P + 1, NS = N + 1;
     constexpr int RM = Q / 16, CQ = Q / 16, CP = P / 16, CN = N / 16;
     extern __shared__ float sm[];
     double *redd = reinterpret_cast<double *>(sm);   // [2]: <g, h>, dA (8-byte aligned at the start)
@@ -665,7 +668,7 @@ __global__ void __launch_bounds__(kCT, 1) bwd_chunk_grad(BwdCParams p) {
         redd[tid] = 0.0;
         red[tid] = 0.f;
     }
-    chunk_cum(p.dt + tok0 * p.H + h, p.H, Ah, L, cum);
+    chunk_cum<Q>(p.dt + tok0 * p.H + h, p.H, Ah, L, cum);
     if (tid < Q) {
         wv[tid] = expf(cum[Q - 1] - cum[tid]);
         ev[tid] = expf(cum[tid]);
@@ -785,33 +788,35 @@ __global__ void __launch_bounds__(kCT, 1) bwd_chunk_grad(BwdCParams p) {
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) ghd += __shfl_xor_sync(0xffffffffu, ghd, o);
         if ((tid & 31) == 0) atomicAdd(redd + 0, ghd);
-        // exclusive prefix sums along each row of K: four threads per row, 16 entries each
-        static_assert(Q * 4 == kCT, "four threads per row of K");
-        const int i = tid >> 2, part = tid & 3;
-        float loc[Q / 4];
+        // exclusive prefix sums along each row of K: TPR threads per row, Q / TPR entries each
+        constexpr int TPR = kCT / Q, EPT = Q / TPR;
+        static_assert(TPR * Q == kCT && TPR <= 32, "whole rows of K per warp");
+        const int i = tid / TPR, part = tid % TPR;
+        float loc[EPT];
         float run = 0.f;
 #pragma unroll
-        for (int jj = 0; jj < Q / 4; ++jj) {
+        for (int jj = 0; jj < EPT; ++jj) {
             loc[jj] = run;
-            run += sK[i * QS + part * (Q / 4) + jj];
+            run += sK[i * QS + part * EPT + jj];
         }
         float v = run;
 #pragma unroll
-        for (int o = 1; o < 4; o <<= 1) {
-            const float u = __shfl_up_sync(0xffffffffu, v, o, 4);
+        for (int o = 1; o < TPR; o <<= 1) {
+            const float u = __shfl_up_sync(0xffffffffu, v, o, TPR);
             if (part >= o) v += u;
         }
         const float off = v - run;
 #pragma unroll
-        for (int jj = 0; jj < Q / 4; ++jj) sK[i * QS + part * (Q / 4) + jj] = loc[jj] + off;
+        for (int jj = 0; jj < EPT; ++jj) sK[i * QS + part * EPT + jj] = loc[jj] + off;
     }
     __syncthreads();
 
-    // rc_k, four threads per token (fp32 partial sums, combined in double); ddt, dA and dD
+    // rc_k, TPR threads per token (fp32 partial sums, combined in double); ddt, dA and dD
     {
-        const int k = tid >> 2, part = tid & 3;
+        constexpr int TPR = kCT / Q;
+        const int k = tid / TPR, part = tid % TPR;
         float cs = 0.f, es = 0.f, ws = 0.f;
-        for (int ii = part; ii < Q; ii += 4) {
+        for (int ii = part; ii < Q; ii += TPR) {
             if (ii >= k) {
                 cs += sK[ii * QS + k];
                 es += eu[ii];
@@ -820,8 +825,8 @@ __global__ void __launch_bounds__(kCT, 1) bwd_chunk_grad(BwdCParams p) {
             }
         }
         double rc = (double)cs + (double)es + (double)ws;
-        rc += __shfl_xor_sync(0xffffffffu, rc, 1);
-        rc += __shfl_xor_sync(0xffffffffu, rc, 2);
+#pragma unroll
+        for (int o = 1; o < TPR; o <<= 1) rc += __shfl_xor_sync(0xffffffffu, rc, o);
         rc += exp((double)cum[Q - 1]) * redd[0];
         double da = 0.0;
         if (part == 0 && k < L) {
@@ -893,13 +898,16 @@ cudaError_t launch_all(const Problem &p, const BwdParams &bp, const BwdLayout &l
 }
 
 // ---- chunked path: host side ----
+int chunk_q(const Problem &p) { return p.N > 128 ? chunk_len<256>() : chunk_len<128>(); }
+
 // the chunked path's domain: scalar A at the head dims its kernels are built for
 bool chunked_applies(const Problem &p) {
-    if (p.a_mode != SSD_A_SCALAR || p.P != 64 || (p.N != 64 && p.N != 128)) return false;
-    if (p.H > 65535 || p.b > 65535 || (p.T + kQc - 1) / kQc > (int64_t)INT32_MAX) return false;
+    if (p.a_mode != SSD_A_SCALAR || p.P != 64 || (p.N != 64 && p.N != 128 && p.N != 256)) return false;
+    const int Q = chunk_q(p);
+    if (p.H > 65535 || p.b > 65535 || (p.T + Q - 1) / Q > (int64_t)INT32_MAX) return false;
     Problem q = p;
-    q.Q = kQc;
-    q.nc = (p.T + kQc - 1) / kQc;
+    q.Q = Q;
+    q.nc = (p.T + Q - 1) / Q;
     return generic_supports(q);
 }
 
@@ -910,7 +918,8 @@ struct BwdCLayout {
 
 BwdCLayout bwdc_layout(const Problem &p) {
     BwdCLayout l;
-    l.nc = (p.T + kQc - 1) / kQc;
+    const int Q = chunk_q(p);
+    l.nc = (p.T + Q - 1) / Q;
     const size_t tokh = (size_t)(p.b * p.T * p.H), np = (size_t)(p.b * p.H * l.nc * p.N * p.P);
     l.off_cs = kStatusBytes;
     l.off_st = align_up(l.off_cs + sizeof(float) * (size_t)(p.b * p.H * l.nc), 256);
@@ -918,20 +927,20 @@ BwdCLayout bwdc_layout(const Problem &p) {
     l.off_dbh = align_up(l.off_g + sizeof(float) * np, 256);
     l.off_dch = align_up(l.off_dbh + sizeof(float) * tokh * p.N, 256);
     l.off_cb = align_up(l.off_dch + sizeof(float) * tokh * p.N, 256);
-    l.total = align_up(l.off_cb + sizeof(float) * (size_t)(p.b * l.nc * p.G) * kQc * kQc, 256);
+    l.total = align_up(l.off_cb + sizeof(float) * (size_t)(p.b * l.nc * p.G) * Q * Q, 256);
     return l;
 }
 
 template <typename IO, int N>
 cudaError_t launch_chunked_typed(const Problem &p, const BwdCParams &cp, cudaStream_t s) {
-    constexpr int P = 64;
-    const size_t sm_r = sizeof(float) * (size_t)(2 * kQc * N + 2 * kQc * P + 3 * kQc);
+    constexpr int P = 64, Q = chunk_len<N>();
+    const size_t sm_r = sizeof(float) * (size_t)(2 * Q * N + 2 * Q * P + 3 * Q);
     const size_t sm_g = sizeof(float) * chunk_grad_floats<N, P>();
     cudaError_t e = cudaFuncSetAttribute(bwd_chunk_sr<IO, N, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_r);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(bwd_chunk_grad<IO, N, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_g);
     if (e != cudaSuccess) return e;
-    const size_t sm_cb = sizeof(float) * (size_t)(2 * kQc * (N + 1));
+    const size_t sm_cb = sizeof(float) * (size_t)(2 * Q * (N + 1));
     if ((e = cudaFuncSetAttribute(bwd_chunk_cb<IO, N>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_cb)) !=
         cudaSuccess)
         return e;
@@ -941,7 +950,7 @@ cudaError_t launch_chunked_typed(const Problem &p, const BwdCParams &cp, cudaStr
     // the state entering every chunk: the generic forward's state passing, in place
     {
         Problem q = p;
-        q.Q = kQc;
+        q.Q = Q;
         q.nc = cp.nc;
         q.y = nullptr;
         q.final_state = nullptr;
@@ -976,7 +985,9 @@ cudaError_t chunked_launch(const Problem &p, const BwdGrads &gr, char *base, cud
     cp.nc = (int)l.nc;
     const bool bf = p.io_dtype == SSD_DTYPE_BF16;
     if (p.N == 64) e = bf ? launch_chunked_typed<__nv_bfloat16, 64>(p, cp, s) : launch_chunked_typed<float, 64>(p, cp, s);
-    else e = bf ? launch_chunked_typed<__nv_bfloat16, 128>(p, cp, s) : launch_chunked_typed<float, 128>(p, cp, s);
+    else if (p.N == 128)
+        e = bf ? launch_chunked_typed<__nv_bfloat16, 128>(p, cp, s) : launch_chunked_typed<float, 128>(p, cp, s);
+    else e = bf ? launch_chunked_typed<__nv_bfloat16, 256>(p, cp, s) : launch_chunked_typed<float, 256>(p, cp, s);
     if (e != cudaSuccess) return e;
     // dB, dC: the per-head sums over each group's heads
     BwdParams bp;

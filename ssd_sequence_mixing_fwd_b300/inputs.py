@@ -126,15 +126,21 @@ def algorithmic_bytes_bwd(w: Workload) -> int:
 
 
 def bwd_chunked_applies(w: Workload) -> bool:
-    """Whether ssd_bwd takes its chunked path (scalar A, P 64, N 64 or 128) for ``w``."""
-    return w.a_mode == "scalar" and w.P == 64 and w.N in (64, 128)
+    """Whether ssd_bwd takes its chunked path (scalar A, P 64, N 64, 128 or 256) for ``w``."""
+    return w.a_mode == "scalar" and w.P == 64 and w.N in (64, 128, 256)
 
 
-def algorithmic_flops_bwd(w: Workload, Q: int = 64) -> float:
+def bwd_chunk_len(w: Workload) -> int:
+    """Tokens per chunk of the chunked backward: 64, or 32 at N 256."""
+    return 32 if w.N > 128 else 64
+
+
+def algorithmic_flops_bwd(w: Workload, Q: int = None) -> float:
     """Causal work of the chunked backward on Q-token chunks (every product a multiply-add
     pair): per chunk and head, dY X^T, S^T dY, G B and G^T C on the causal triangle
     (Q^2 N + Q^2 P) and the five rank-N products B g, dY h^T, X g^T, C^T (e o dY) and the
     chunk state B^T (w o X) (5 Q N P); per chunk and B/C group, C B^T (Q^2 N / 2)."""
+    Q = bwd_chunk_len(w) if Q is None else Q
     nc = -(-w.T // Q)
     per_head = Q * Q * w.N + Q * Q * w.P + 5 * Q * w.N * w.P
     per_group = 0.5 * Q * Q * w.N

@@ -83,9 +83,13 @@ CASES = [
                                      seed=723)),
     ("chunked_bf16_N128_G2_T200", Workload("t", b=2, T=200, H=6, P=64, N=128, G=2, Q=256, D="none",
                                            init_std=0.1, seed=724)),
-    # the long-sequence head dims (N 256, one head per B/C group): the recurrence path, 16 slices
-    ("scalar_bf16_N256_G8", Workload("t", b=1, T=150, H=8, P=64, N=256, G=8, Q=128, D="none", init_std=0.1,
-                                     seed=725)),
+    # the long-sequence head dims (N 256, one head per B/C group): the chunked path on 32-token chunks
+    ("chunked_bf16_N256_G8", Workload("t", b=1, T=150, H=8, P=64, N=256, G=8, Q=128, D="none", init_std=0.1,
+                                      seed=725)),
+    ("chunked_f32_N256_G2", Workload("t", b=2, T=77, H=4, P=64, N=256, G=2, Q=128, dtype="f32", D="normal",
+                                     init_std=0.2, seed=726)),
+    # the recurrence path at N 256 (P 32 is outside the chunked path)
+    ("scalar_bf16_P32_N256", Workload("t", b=1, T=90, H=2, P=32, N=256, G=1, Q=128, D="normal", seed=727)),
 ]
 
 
