@@ -49,6 +49,8 @@ SMALL = [
              init_std=0.3, seed=504),
     Workload("s5", b=1, T=64, H=8, P=64, N=256, G=8, Q=128, D="none", init_std=0.1, seed=505),
     Workload("s6", b=1, T=33, H=2, P=256, N=64, G=1, Q=256, D="normal", seed=506),
+    # bf16 with a 16-wide state at P 64 (the bench's state-16 comparison runs this configuration)
+    Workload("s7", b=2, T=180, H=4, P=64, N=16, G=1, Q=64, D="normal", seed=507),
 ]
 
 
