@@ -211,9 +211,10 @@ SSD_API int ssd_decode_step(const ssd_dims *dims,
  * weighs; the pages give no backward, so this is the chain rule of the
  * recurrence of "The recurrence as one matrix").  CUDA cores, fp32
  * arithmetic, two paths:
- *  - scalar A with P == 64 and N in {64, 128, 256}: the chunked algorithm
- *    run backwards on Q-token chunks (Q = 64; 32 at N = 256) -- the state
- *    entering every chunk (the
+ *  - scalar A with P in {64, 128} and N in {64, 128, 256} (not P = 128 with
+ *    N = 256): the chunked algorithm run backwards on Q-token chunks (Q = 64;
+ *    32 at N = 256 and at P = N = 128, where the 64-token product kernel's
+ *    shared memory would not fit) -- the state entering every chunk (the
  *    generic forward's chunk-state kernels), the adjoint at every chunk's
  *    end (a reverse scan over chunks), then per chunk and head the dense
  *    products of the quadratic form and the rank-N terms;

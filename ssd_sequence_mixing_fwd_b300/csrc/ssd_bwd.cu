@@ -345,8 +345,16 @@ __global__ void __launch_bounds__(256) bwd_finish_params(BwdParams p) {
 // bwd_state_reverse runs the adjoint backwards over the chunks (each chunk's end adjoint
 // left in place, and dinit); bwd_chunk_grad does the rest, one CTA per chunk and head,
 // every product in exact fp32 on the CUDA cores.
-// tokens per chunk: 64, or 32 at N = 256 (the product kernel's shared memory then still fits)
-template <int N> constexpr int chunk_len() { return N > 128 ? 32 : 64; }
+// shared-memory floats of the product kernel (bwd_chunk_grad) for Q-token chunks
+constexpr size_t grad_floats(int N, int P, int Q) {
+    return 8 + (size_t)2 * Q * (P + 1) + 2 * Q * (N + 1) + 2 * N * (P + 1) + 3 * Q * (Q + 1) + 5 * Q;
+}
+constexpr size_t kSmemFloats = 227 * 1024 / 4;
+// tokens per chunk: 64 where the product kernel's shared memory fits, else 32 (0: neither)
+constexpr int chunk_len_of(int N, int P) {
+    return grad_floats(N, P, 64) <= kSmemFloats ? 64 : grad_floats(N, P, 32) <= kSmemFloats ? 32 : 0;
+}
+template <int N, int P> constexpr int chunk_len() { return chunk_len_of(N, P); }
 constexpr int kCT = 256;          // threads of the chunk kernels
 
 struct BwdCParams {
@@ -432,9 +440,9 @@ template <int RM, int CN> __device__ __forceinline__ void zero(float (&acc)[RM][
 template <int RM, int CN>
 __device__ __forceinline__ void mm(float (&acc)[RM][CN], const float *A, int am, int ak, const float *Bm, int bk,
                                    int bn, int K, int tm, int tn);
-template <typename IO, int N>
+template <typename IO, int N, int P>
 __global__ void __launch_bounds__(kCT) bwd_chunk_cb(BwdCParams p) {
-    constexpr int Q = chunk_len<N>(), NS = N + 1, RM = Q / 16, CQ = Q / 16;
+    constexpr int Q = chunk_len<N, P>(), NS = N + 1, RM = Q / 16, CQ = Q / 16;
     extern __shared__ float sm[];
     float *sB = sm, *sC = sm + Q * NS;
     const int c = blockIdx.x, g = blockIdx.y, bi = blockIdx.z, tid = threadIdx.x;
@@ -460,8 +468,8 @@ __global__ void __launch_bounds__(kCT) bwd_chunk_cb(BwdCParams p) {
 // (tm, tn): state rows tm + 16 a, columns tn + 16 j), whose loads are one wavefront each.  Two
 // CTAs per SM (99 KB of shared memory each at N 128; registers capped at 128 for it).
 template <typename IO, int N, int P>
-__global__ void __launch_bounds__(kCT, N > 128 ? 1 : 2) bwd_chunk_sr(BwdCParams p) {
-    constexpr int Q = chunk_len<N>();
+__global__ void __launch_bounds__(kCT, N * P > 8192 ? 1 : 2) bwd_chunk_sr(BwdCParams p) {
+    constexpr int Q = chunk_len<N, P>();
     extern __shared__ float sm[];
     float *sCe = sm;                  // [Q][N] e o C
     float *sBw = sCe + Q * N;         // [Q][N] w o B
@@ -626,13 +634,12 @@ __device__ __forceinline__ float sum16(float v) {
 
 template <int N, int P>
 constexpr size_t chunk_grad_floats() {
-    constexpr int Q = chunk_len<N>();
-    return 8 + (size_t)2 * Q * (P + 1) + 2 * Q * (N + 1) + 2 * N * (P + 1) + 3 * Q * (Q + 1) + 5 * Q;
+    return grad_floats(N, P, chunk_len<N, P>());
 }
 
 template <typename IO, int N, int P>
 __global__ void __launch_bounds__(kCT, 1) bwd_chunk_grad(BwdCParams p) {
-    constexpr int Q = chunk_len<N>(), QS = Q + 1, PS = P + 1, NS = N + 1;
+    constexpr int Q = chunk_len<N, P>(), QS = Q + 1, PS = P + 1, NS = N + 1;
     constexpr int RM = Q / 16, CQ = Q / 16, CP = P / 16, CN = N / 16;
     extern __shared__ float sm[];
     double *redd = reinterpret_cast<double *>(sm);   // [2]: <g, h>, dA (8-byte aligned at the start)
@@ -898,12 +905,14 @@ cudaError_t launch_all(const Problem &p, const BwdParams &bp, const BwdLayout &l
 }
 
 // ---- chunked path: host side ----
-int chunk_q(const Problem &p) { return p.N > 128 ? chunk_len<256>() : chunk_len<128>(); }
+int chunk_q(const Problem &p) { return chunk_len_of((int)p.N, (int)p.P); }
 
 // the chunked path's domain: scalar A at the head dims its kernels are built for
 bool chunked_applies(const Problem &p) {
-    if (p.a_mode != SSD_A_SCALAR || p.P != 64 || (p.N != 64 && p.N != 128 && p.N != 256)) return false;
+    if (p.a_mode != SSD_A_SCALAR || (p.P != 64 && p.P != 128)) return false;
+    if (p.N != 64 && p.N != 128 && p.N != 256) return false;
     const int Q = chunk_q(p);
+    if (Q == 0) return false;
     if (p.H > 65535 || p.b > 65535 || (p.T + Q - 1) / Q > (int64_t)INT32_MAX) return false;
     Problem q = p;
     q.Q = Q;
@@ -931,9 +940,10 @@ BwdCLayout bwdc_layout(const Problem &p) {
     return l;
 }
 
-template <typename IO, int N>
+template <typename IO, int N, int P>
 cudaError_t launch_chunked_typed(const Problem &p, const BwdCParams &cp, cudaStream_t s) {
-    constexpr int P = 64, Q = chunk_len<N>();
+    constexpr int Q = chunk_len<N, P>();
+    static_assert(Q > 0, "an instantiated head shape has a chunk length");
     const size_t sm_r = sizeof(float) * (size_t)(2 * Q * N + 2 * Q * P + 3 * Q);
     const size_t sm_g = sizeof(float) * chunk_grad_floats<N, P>();
     cudaError_t e = cudaFuncSetAttribute(bwd_chunk_sr<IO, N, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_r);
@@ -941,10 +951,10 @@ cudaError_t launch_chunked_typed(const Problem &p, const BwdCParams &cp, cudaStr
         e = cudaFuncSetAttribute(bwd_chunk_grad<IO, N, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_g);
     if (e != cudaSuccess) return e;
     const size_t sm_cb = sizeof(float) * (size_t)(2 * Q * (N + 1));
-    if ((e = cudaFuncSetAttribute(bwd_chunk_cb<IO, N>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_cb)) !=
+    if ((e = cudaFuncSetAttribute(bwd_chunk_cb<IO, N, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_cb)) !=
         cudaSuccess)
         return e;
-    bwd_chunk_cb<IO, N><<<dim3((unsigned)cp.nc, (unsigned)p.G, (unsigned)p.b), kCT, sm_cb, s>>>(cp);
+    bwd_chunk_cb<IO, N, P><<<dim3((unsigned)cp.nc, (unsigned)p.G, (unsigned)p.b), kCT, sm_cb, s>>>(cp);
     const dim3 grid((unsigned)cp.nc, (unsigned)p.H, (unsigned)p.b);
     bwd_chunk_sr<IO, N, P><<<grid, kCT, sm_r, s>>>(cp);
     // the state entering every chunk: the generic forward's state passing, in place
@@ -984,10 +994,11 @@ cudaError_t chunked_launch(const Problem &p, const BwdGrads &gr, char *base, cud
     cp.b = (int)p.b; cp.T = (int)p.T; cp.H = (int)p.H; cp.G = (int)p.G; cp.N = (int)p.N; cp.P = (int)p.P;
     cp.nc = (int)l.nc;
     const bool bf = p.io_dtype == SSD_DTYPE_BF16;
-    if (p.N == 64) e = bf ? launch_chunked_typed<__nv_bfloat16, 64>(p, cp, s) : launch_chunked_typed<float, 64>(p, cp, s);
-    else if (p.N == 128)
-        e = bf ? launch_chunked_typed<__nv_bfloat16, 128>(p, cp, s) : launch_chunked_typed<float, 128>(p, cp, s);
-    else e = bf ? launch_chunked_typed<__nv_bfloat16, 256>(p, cp, s) : launch_chunked_typed<float, 256>(p, cp, s);
+#define SSD_CHUNKED(N_, P_) \
+    (bf ? launch_chunked_typed<__nv_bfloat16, N_, P_>(p, cp, s) : launch_chunked_typed<float, N_, P_>(p, cp, s))
+    if (p.P == 64) e = p.N == 64 ? SSD_CHUNKED(64, 64) : p.N == 128 ? SSD_CHUNKED(128, 64) : SSD_CHUNKED(256, 64);
+    else e = p.N == 64 ? SSD_CHUNKED(64, 128) : SSD_CHUNKED(128, 128);
+#undef SSD_CHUNKED
     if (e != cudaSuccess) return e;
     // dB, dC: the per-head sums over each group's heads
     BwdParams bp;

@@ -125,14 +125,23 @@ def algorithmic_bytes_bwd(w: Workload) -> int:
     return by
 
 
-def bwd_chunked_applies(w: Workload) -> bool:
-    """Whether ssd_bwd takes its chunked path (scalar A, P 64, N 64, 128 or 256) for ``w``."""
-    return w.a_mode == "scalar" and w.P == 64 and w.N in (64, 128, 256)
+def _bwd_grad_floats(N: int, P: int, Q: int) -> int:
+    return 8 + 2 * Q * (P + 1) + 2 * Q * (N + 1) + 2 * N * (P + 1) + 3 * Q * (Q + 1) + 5 * Q
 
 
 def bwd_chunk_len(w: Workload) -> int:
-    """Tokens per chunk of the chunked backward: 64, or 32 at N 256."""
-    return 32 if w.N > 128 else 64
+    """Tokens per chunk of the chunked backward: 64 where its product kernel's shared memory
+    (227 KB) fits, else 32; 0 where neither fits."""
+    for Q in (64, 32):
+        if _bwd_grad_floats(w.N, w.P, Q) <= 227 * 1024 // 4:
+            return Q
+    return 0
+
+
+def bwd_chunked_applies(w: Workload) -> bool:
+    """Whether ssd_bwd takes its chunked path (scalar A, P 64 or 128, N 64, 128 or 256, and a
+    chunk length whose product kernel fits) for ``w``."""
+    return w.a_mode == "scalar" and w.P in (64, 128) and w.N in (64, 128, 256) and bwd_chunk_len(w) > 0
 
 
 def algorithmic_flops_bwd(w: Workload, Q: int = None) -> float:

@@ -202,16 +202,18 @@ def a256(v):
 
 
 @pytest.mark.parametrize("kw", [dict(b=2, T=100, H=4, P=64, N=128), dict(b=1, T=64, H=2, P=64, N=64),
-                                dict(b=3, T=1, H=6, P=64, N=128, G=3), dict(b=1, T=100, H=4, P=64, N=256)])
+                                dict(b=3, T=1, H=6, P=64, N=128, G=3), dict(b=1, T=100, H=4, P=64, N=256),
+                                dict(b=1, T=100, H=4, P=128, N=64), dict(b=2, T=70, H=2, P=128, N=128)])
 def test_backward_workspace_of_the_chunked_path(lib, kw):
-    # scalar A at P 64, N 64 / 128 / 256 on Q-token chunks (Q = 64; 32 at N 256): states and
+    # scalar A at P 64 / 128, N 64 / 128 / 256 on Q-token chunks (Q = 64; 32 at N 256 and at
+    # P = N = 128): states and
     # adjoints (b H ceil(T/Q) N P fp32 each), the chunk sums, per-head dB and dC (b T H N fp32
     # each), C B^T per chunk and group (b ceil(T/Q) G Q Q fp32), every region rounded up to 256
     # bytes
     d = dims(path="auto", **kw)
     b, T, H, P, N = kw["b"], kw["T"], kw["H"], kw["P"], kw["N"]
     G = kw.get("G", 2)
-    Q = 32 if N > 128 else 64
+    Q = 32 if N > 128 or (P == 128 and N == 128) else 64
     nc = -(-T // Q)
     want = 256 + a256(4 * b * H * nc) + a256(4 * b * H * nc * N * P) * 2 + a256(4 * b * T * H * N) * 2
     want += a256(4 * b * nc * G * Q * Q)

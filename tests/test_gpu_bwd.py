@@ -88,6 +88,11 @@ CASES = [
                                       seed=725)),
     ("chunked_f32_N256_G2", Workload("t", b=2, T=77, H=4, P=64, N=256, G=2, Q=128, dtype="f32", D="normal",
                                      init_std=0.2, seed=726)),
+    # P 128: 64-token chunks at N 64, 32-token chunks at N 128
+    ("chunked_f32_P128_N64", Workload("t", b=2, T=90, H=2, P=128, N=64, G=1, Q=64, dtype="f32", D="normal",
+                                      init_std=0.2, seed=728)),
+    ("chunked_bf16_P128_N128_G2", Workload("t", b=1, T=170, H=4, P=128, N=128, G=2, Q=128, D="none",
+                                           init_std=0.1, seed=729)),
     # the recurrence path at N 256 (P 32 is outside the chunked path)
     ("scalar_bf16_P32_N256", Workload("t", b=1, T=90, H=2, P=32, N=256, G=1, Q=128, D="normal", seed=727)),
 ]
