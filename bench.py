@@ -146,7 +146,7 @@ def time_backward(ssd, torch, w, d, dev, stream, flush, peaks, args):
     CUDA events on the launching stream, L2 flushed before each call; plus the fp64 backward
     oracle on a bounded sample of the same workload on the host cores."""
     from ssd_sequence_mixing_fwd_b300.inputs import (algorithmic_bytes_bwd, algorithmic_flops_bwd,
-                                                     bwd_chunked_applies, make_inputs)
+                                                     bwd_chunk_len, bwd_chunked_applies, make_inputs)
     g = torch.Generator(device="cpu").manual_seed(4242)
     dy = torch.randn(d["x"].shape, generator=g).to(d["x"].dtype).to(dev)
     b, T, H, P = d["x"].shape
@@ -170,7 +170,7 @@ def time_backward(ssd, torch, w, d, dev, stream, flush, peaks, args):
     ms = sum(times) / len(times)
     by = algorithmic_bytes_bwd(w)
     chunked = bwd_chunked_applies(w)
-    ent = {"path": ("chunked: 64-token chunks, fp32 products on the CUDA cores" if chunked
+    ent = {"path": ("chunked: %d-token chunks, fp32 products on the CUDA cores" % bwd_chunk_len(w) if chunked
                     else "token recurrence on the CUDA cores"),
            "call_ms": ms, "tokens_per_s": w.tokens / (ms / 1e3),
            "workspace_bytes": ws.numel(),
