@@ -234,8 +234,9 @@ SSD_API int ssd_decode_step(const ssd_dims *dims,
  * dA and dD are sums over chunks (or token ranges) added with fp32 atomics,
  * so they may differ in the last bits from one call to the next; every other
  * output is reproducible.
- * dims->path must be SSD_PATH_AUTO or SSD_PATH_GENERIC (SSD_ERR_UNSUPPORTED
- * otherwise); the backward takes 4 <= P <= 128.  Every pointer 16-byte
+ * dims->path must be SSD_PATH_AUTO (the chunked path where it applies, the
+ * recurrence elsewhere) or SSD_PATH_GENERIC (the recurrence for every dims);
+ * SSD_ERR_UNSUPPORTED otherwise.  The backward takes 4 <= P <= 128.  Every pointer 16-byte
  * aligned; workspace >= ssd_bwd_workspace_size bytes, 256-byte aligned
  * (chunked path, Q as above: two fp32 arrays of b*H*ceil(T/Q)*N*P floats --
  * the states and the adjoints -- plus 2*b*T*H*N floats of per-head dB and dC

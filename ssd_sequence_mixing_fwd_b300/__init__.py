@@ -287,19 +287,20 @@ def ssd_bwd_workspace_size(dims):
 
 
 def ssd_bwd(x, dt, A, B, C, D=None, init_state=None, dy=None, dfinal=None, want_dD=True, want_dinit=True,
-            workspace=None, stream=None):
+            workspace=None, stream=None, path="auto"):
     """Gradients of ``sum y*dy + sum final_state*dfinal`` for the map :func:`ssd_fwd` computes.
 
     Returns a dict with dx (like x), ddt (b,T,H) fp32, dA (like A) fp32, dB and dC (like B) in
     the io dtype, dD (H) fp32 (None unless ``want_dD``) and dinit (b,H,N,P) fp32 (None unless
     ``want_dinit``).  ``dy`` has x's shape and dtype; ``dfinal`` is (b,H,N,P) fp32 or None.
+    ``path``: "auto" (the chunked path where it applies) or "generic" (the token recurrence).
     Asynchronous on the current stream."""
     import torch
     if dy is None or dy.shape != x.shape or dy.dtype != x.dtype or not dy.is_cuda or not dy.is_contiguous():
         raise ValueError("dy must be a contiguous CUDA tensor with x's shape and dtype")
     if dfinal is not None and (dfinal.dtype != torch.float32 or not dfinal.is_cuda or not dfinal.is_contiguous()):
         raise ValueError("dfinal must be a contiguous float32 CUDA tensor")
-    dims, args, _, _, _, s = _marshal(x, dt, A, B, C, D, init_state, 256, False, "auto", x, None,
+    dims, args, _, _, _, s = _marshal(x, dt, A, B, C, D, init_state, 256, False, path, x, None,
                                       _NO_WORKSPACE, stream)
     b, T, H, P = x.shape
     G, N = B.shape[2], B.shape[3]

@@ -187,7 +187,7 @@ extern "C" int ssd_bwd_workspace_size(const ssd_dims *dims, size_t *bytes) {
     Problem p;
     const int st = bwd_check(dims, &p);
     if (st != SSD_OK) return st;
-    *bytes = bwd_workspace_bytes(p);
+    *bytes = bwd_workspace_bytes(p, dims->path == SSD_PATH_AUTO);
     return SSD_OK;
 }
 
@@ -204,7 +204,8 @@ extern "C" int ssd_bwd(const ssd_dims *dims, const void *x, const float *dt, con
     const void *ptrs[] = {x, dt, A, B, C, D, init_state, dy, dfinal, dx, ddt, dA, dB, dC, dD, dinit};
     for (const void *q : ptrs)
         if (q && !aligned16(q)) return SSD_ERR_ALIGNMENT;
-    const size_t need = bwd_workspace_bytes(p);
+    const bool chunked_ok = dims->path == SSD_PATH_AUTO;
+    const size_t need = bwd_workspace_bytes(p, chunked_ok);
     if (!workspace || workspace_bytes < need) return SSD_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SSD_ERR_ALIGNMENT;
     p.x = x; p.dt = dt; p.A = A; p.B = B; p.C = C; p.D = D; p.init = init_state;
@@ -222,7 +223,7 @@ extern "C" int ssd_bwd(const ssd_dims *dims, const void *x, const float *dt, con
         return note_cuda(e);
     }
     BwdGrads g{dy, dfinal, dx, ddt, dA, dB, dC, dD, dinit};
-    return note_cuda(bwd_launch(p, g, workspace, s));
+    return note_cuda(bwd_launch(p, g, workspace, s, chunked_ok));
 }
 
 // The linear form (ssd_scan) and its one-token case (ssd_decode_step): same argument checks as

@@ -1022,13 +1022,13 @@ bool bwd_supports(const Problem &p) {
     return true;
 }
 
-size_t bwd_workspace_bytes(const Problem &p) {
-    return chunked_applies(p) ? bwdc_layout(p).total : bwd_layout(p).total;
+size_t bwd_workspace_bytes(const Problem &p, bool chunked_ok) {
+    return chunked_ok && chunked_applies(p) ? bwdc_layout(p).total : bwd_layout(p).total;
 }
 
-cudaError_t bwd_launch(const Problem &p, const BwdGrads &gr, void *ws, cudaStream_t s) {
+cudaError_t bwd_launch(const Problem &p, const BwdGrads &gr, void *ws, cudaStream_t s, bool chunked_ok) {
     char *base = static_cast<char *>(ws);
-    if (chunked_applies(p)) {
+    if (chunked_ok && chunked_applies(p)) {
         cudaError_t e = cudaMemsetAsync(base, 0, kStatusBytes, s);
         if (e == cudaSuccess) e = cudaMemsetAsync(gr.dA, 0, sizeof(float) * (size_t)p.H, s);
         if (e == cudaSuccess && gr.dD) e = cudaMemsetAsync(gr.dD, 0, sizeof(float) * (size_t)p.H, s);

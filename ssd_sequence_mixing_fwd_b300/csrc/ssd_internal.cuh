@@ -71,8 +71,10 @@ struct BwdGrads {
     float *dinit;          // (b,H,N,P) or null
 };
 bool bwd_supports(const Problem &p);
-size_t bwd_workspace_bytes(const Problem &p);
-cudaError_t bwd_launch(const Problem &p, const BwdGrads &g, void *ws, cudaStream_t s);
+// chunked_ok: the chunked path may be taken where it applies (SSD_PATH_AUTO); else the
+// token recurrence runs
+size_t bwd_workspace_bytes(const Problem &p, bool chunked_ok);
+cudaError_t bwd_launch(const Problem &p, const BwdGrads &g, void *ws, cudaStream_t s, bool chunked_ok);
 
 // ---- linear-form scan (csrc/ssd_scan.cu): no workspace ---------------------
 bool scan_supports(const Problem &p);

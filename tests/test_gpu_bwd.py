@@ -171,3 +171,27 @@ def test_backward_at_the_2p7b_bench_shape(cuda_device):
         if ref["dD"] is not None:
             terms_d = np.abs(dy[:, :, h].double().numpy() * inp["x"][:, :, h].double().numpy()).sum()
             assert abs(got["dD"][h] - ref["dD"][0]) <= 1e-4 * abs(ref["dD"][0]) + 2 * eps * terms_d
+
+
+@pytest.mark.parametrize("dtype,tol", [("f32", 1e-5), ("bf16", 1e-4)])
+def test_chunked_and_recurrence_paths_agree(dtype, tol, cuda_device):
+    """The chunked backward (path "auto") and the token recurrence (path "generic") are two
+    different evaluations of the same gradients: on the same inputs they agree with each other,
+    every output, at the fp32 arithmetic's accuracy (io rounding aside)."""
+    w = Workload("t", b=2, T=150, H=4, P=64, N=128, G=2, Q=128, dtype=dtype, D="normal", init_std=0.2,
+                 seed=731)
+    inp = make_inputs(w)
+    dy, df = cotangents(w, 9, True)
+    d = {k: (None if v is None else v.to(cuda_device)) for k, v in inp.items()}
+    args = (d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["init_state"], dy.to(cuda_device),
+            df.to(cuda_device))
+    a = ssd.ssd_bwd(*args, path="auto")
+    r = ssd.ssd_bwd(*args, path="generic")
+    torch.cuda.synchronize()
+    dims = ssd.make_dims(w.b, w.T, w.H, w.P, w.N, w.G, w.Q, dtype=dtype)
+    assert ssd.ssd_bwd_workspace_size(dims) != ssd.ssd_bwd_workspace_size(
+        ssd.make_dims(w.b, w.T, w.H, w.P, w.N, w.G, w.Q, dtype=dtype, path="generic"))   # two layouts
+    for k in ("dx", "ddt", "dA", "dB", "dC", "dD", "dinit"):
+        ga, gr = a[k].float().cpu().numpy(), r[k].float().cpu().numpy()
+        lim = 2e-3 if (dtype == "bf16" and k in ("dx", "dB", "dC")) else tol
+        assert rel(ga, gr) <= lim, (k, rel(ga, gr))
